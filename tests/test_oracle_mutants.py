@@ -1,0 +1,54 @@
+"""Plant plausible mistakes in copies of the oracle source and require the
+pins to catch every one.  This shows the pins constrain each part of the
+oracle: dequantisation, alignment, both projections, the activation and the
+combine."""
+import os
+
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+MUTANTS = [
+    ("zero point 7", "(double)(code - 8)", "(double)(code - 7)"),
+    ("nibble order swapped", "(kk & 1) ? (byte >> 4) : (byte & 0x0F)",
+     "(kk & 1) ? (byte & 0x0F) : (byte >> 4)"),
+    ("first group scale only", "s[n * (K / 32) + kk / 32]", "s[n * (K / 32)]"),
+    ("silu sign", "exp(-v)", "exp(v)"),
+    ("gate and up swapped", "a[n] = silu(g) * u;", "a[n] = silu(u) * g;"),
+    ("up rows interleaved", "weight_at(q13, sc13, H, I + n, h)",
+     "weight_at(q13, sc13, H, 2 * n + 1 < 2 * I ? 2 * n + 1 : n, h)"),
+    ("down projection transposed", "weight_at(q2, sc2, I, hh, n)",
+     "weight_at(q2, sc2, I, n, hh % I)"),
+    ("first hidden element dropped", "for (int64_t h = 0; h < H; ++h)",
+     "for (int64_t h = 1; h < H; ++h)"),
+    ("combine ignores topk_w", "acc += (double)topk_w[t * k + j] * yrow",
+     "acc += 1.0 * yrow"),
+    ("combine reads slot 0 only", "int32_t pos = inv_perm[t * k + j];",
+     "int32_t pos = inv_perm[t * k];"),
+    ("unstable placement", "int32_t pos = offsets[e] + counts[e];",
+     "int32_t pos = offsets[e + 1] - 1 - counts[e];"),
+    ("token index from slot modulo", "int64_t t = f / k;", "int64_t t = f % k;"),
+]
+
+
+def _run_pins(orc):
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(orc)
+        except AssertionError as exc:
+            failed.append((pin.__name__, str(exc)[:80]))
+    return failed
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new):
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) >= 1, f"mutation anchor not found: {old!r}"
+    mutated = src.replace(old, new)
+    path = tmp_path / "mutant.c"
+    path.write_text(mutated)
+    so = oracle.compile_source(str(path), str(tmp_path / "libmutant.so"))
+    failed = _run_pins(oracle.Oracle(so))
+    assert failed, f"mutant '{name}' passed every pin"
