@@ -1,0 +1,417 @@
+#!/usr/bin/env python
+"""Benchmark of the W4A16 MoE layer forward on GB300.
+
+One step = one forward call per batch size of the workload (default: the
+decode sweep M in {1, 9, 90} of an E=384, H=7168, I=2048, top-8, INT4 g32
+layer), inputs already resident in HBM, L2 flushed before every step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode|plateau|prefill|second|toy]
+                  [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the plain CPU
+oracle on a bounded sample of the same workload instead.  Under torchrun
+(N > 1) every rank runs an independent replica of the workload on its own GPU
+(the layer forward has no exchange step); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = ("MoE layer µs/call & tokens/s vs M (1–16384); HBM GB/s or tensor-pipe % of peak")
+CONFIGS = {"decode": synth.DECODE, "plateau": synth.PLATEAU, "prefill": synth.PREFILL,
+           "second": synth.SECOND, "toy": synth.TOY}
+# The pages' sweep on one RTX PRO 6000 (sm_120), context only: ms per call.
+PAGES_MS = {1: 0.151, 9: 1.18, 90: 5.19, 256: 7.02, 512: 7.01, 1024: 7.02}
+KERNELS = ["align", "gather", "gemm_gate_up", "gemm_down", "combine"]
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def expert_bytes(L):
+    w13 = 2 * L.I * L.H // 2 + 2 * L.I * (L.H // 32) * 2
+    w2 = L.H * L.I // 2 + L.H * (L.I // 32) * 2
+    return w13, w2
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_sample(wl, batches, max_slots):
+    """A bounded sample of the workload for the oracle: from each batch, the
+    first tokens up to a share of ``max_slots`` slots."""
+    per = max(1, max_slots // max(1, len(batches)))
+    out = []
+    for M, (x, ids, w) in batches.items():
+        t = max(1, min(M, per // wl.layer.k))
+        out.append((M, x[:t], ids[:t], w[:t]))
+    return out
+
+
+def run_oracle(wl, host_w, sample):
+    import oracle
+    L = wl.layer
+    tok = 0
+    t0 = time.perf_counter()
+    for _, x, ids, w in sample:
+        oracle.forward(x, ids, w, *host_w, L.E, L.H, L.I)
+        tok += x.shape[0]
+    return tok, time.perf_counter() - t0
+
+
+def make_batches(wl, seed=0):
+    L = wl.layer
+    out = {}
+    for M in wl.Ms:
+        x = synth.hidden(M, L.H, seed)
+        ids, w = synth.routing(M, L, seed, zipf_s=wl.zipf_s)
+        out[M] = (x, ids, w)
+    return out
+
+
+def describe_sample(sample, wl):
+    parts = [f"{x.shape[0]} of {M} tokens" for M, x, _, _ in sample]
+    return (f"{wl.name}: " + ", ".join(parts) + " (oracle in fp64, all k slots of each "
+            "sampled token)")
+
+
+def reference_arm(args, wl):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    L = wl.layer
+    batches = make_batches(wl)
+    touched = sorted(set(int(e) for _, ids, _ in batches.values() for e in np.unique(ids)))
+    host_w = synth.layer_weights(L, 0, experts=touched)
+    sample = oracle_sample(wl, batches, max_slots=8 * len(wl.Ms))
+    for _ in range(args.warmup):
+        run_oracle(wl, host_w, sample)
+    tok, secs = 0, 0.0
+    for _ in range(args.steps):
+        t, s = run_oracle(wl, host_w, sample)
+        tok += t
+        secs += s
+    value = tok / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "Ms": list(wl.Ms), "E": L.E, "H": L.H, "I": L.I,
+                   "k": L.k, "group": 32, "parallelism": "none (host CPU)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": describe_sample(sample, wl)},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def our_arm(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import quantized_moe_expert_align_gb300 as moe
+    from quantized_moe_expert_align_gb300 import build as lib_build
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    lib_build.build()
+    moe.load()
+    L = wl.layer
+    hbm_peak, tf_peak, peak_kind = peaks()
+
+    # weights: canonical on the host (the oracle's copy), prepacked on the GPU
+    host_w = synth.layer_weights(L, 0)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    q = dev(host_w[0])
+    s = dev(host_w[1].view(np.int16))
+    p13 = moe.prepack(moe.MOE_PACK_W13, q, s)
+    del q, s
+    q = dev(host_w[2])
+    s = dev(host_w[3].view(np.int16))
+    p2 = moe.prepack(moe.MOE_PACK_W2, q, s)
+    del q, s
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+    batches = make_batches(wl)
+    Mmax = max(wl.Ms)
+    ws = moe.Workspace(Mmax, L.k, L.E, L.H, L.I, "cuda")
+    devb = {}
+    for M, (x, ids, w) in batches.items():
+        devb[M] = (dev(x.view(np.int16)).view(torch.bfloat16), dev(ids), dev(w),
+                   torch.empty((M, L.H), dtype=torch.bfloat16, device="cuda"))
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
+
+    def call(M):
+        x, ids, w, out = devb[M]
+        st = moe.moe_w4a16_forward(x, ids, w, p13[0], p13[1], p2[0], p2[1], out, M, L.k, L.E,
+                                   L.H, L.I, ws.buf, stream)
+        if st != moe.MOE_OK:
+            raise moe.MoeError(st, "moe_w4a16_forward")
+
+    def step():
+        for M in wl.Ms:
+            call(M)
+
+    # correctness gate before timing (device status of the last call)
+    step()
+    st, detail = moe.moe_w4a16_get_device_status(ws.buf)
+    if st != moe.MOE_OK:
+        raise moe.MoeError(st, f"device status (detail {detail})")
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, device time per step, L2 flushed between ----
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens_per_step = sum(wl.Ms)
+    value = world * tokens_per_step * args.steps / (total_ms / 1e3)
+    gpu_launches = moe.moe_w4a16_get_diag()["kernels_launched"] * len(wl.Ms) * args.steps
+
+    # ---- per-kernel durations (events between the library's kernels) ----
+    prof_steps = max(3, min(args.steps, 10))
+    per_kernel = {M: np.zeros(5) for M in wl.Ms}
+    for _ in range(prof_steps):
+        for M in wl.Ms:
+            x, ids, w, out = devb[M]
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+            flush.zero_()
+            st = moe.moe_w4a16_forward_profiled(x, ids, w, p13[0], p13[1], p2[0], p2[1], out, M,
+                                                L.k, L.E, L.H, L.I, ws.buf, evs, stream)
+            if st != moe.MOE_OK:
+                raise moe.MoeError(st, "moe_w4a16_forward_profiled")
+            torch.cuda.synchronize()
+            per_kernel[M] += np.array([evs[i].elapsed_time(evs[i + 1]) for i in range(5)])
+    for M in wl.Ms:
+        per_kernel[M] /= prof_steps
+
+    # roofline: the gate+up GEMM streams the touched experts' w13 codes+scales
+    b13, b2 = expert_bytes(L)
+    sweep = []
+    gemm1_bytes = gemm1_ms = 0.0
+    for M in wl.Ms:
+        active = int(np.unique(batches[M][1]).size)
+        k_ms = per_kernel[M]
+        gemm1_bytes += active * b13
+        gemm1_ms += float(k_ms[2])
+        roof_bytes = active * (b13 + b2)
+        flops = 6.0 * M * L.k * L.H * L.I
+        t_roof_ms = 1e3 * max(roof_bytes / (hbm_peak * 1e9), flops / (tf_peak * 1e12))
+        sweep.append({
+            "M": M, "active_experts": active,
+            "kernel_ms": {n: round(float(v), 5) for n, v in zip(KERNELS, k_ms)},
+            "us_per_call_profiled": round(1e3 * float(k_ms.sum()), 2),
+            "roofline_bytes": roof_bytes, "roofline_us": round(1e3 * t_roof_ms, 2),
+            "frac_of_roofline_profiled": round(t_roof_ms / float(k_ms.sum()), 4),
+            "pages_ms_rtx_pro_6000": PAGES_MS.get(M) if L.E == 384 else None,
+        })
+    achieved = gemm1_bytes / (gemm1_ms / 1e3) / 1e9
+
+    # ---- end to end through the C ABI: pinned host inputs and output ----
+    e2e = None
+    host = {}
+    h2d = d2h = 0
+    for M, (x, ids, w) in batches.items():
+        hx = torch.from_numpy(x.view(np.int16)).pin_memory()
+        hid = torch.from_numpy(ids).pin_memory()
+        hw = torch.from_numpy(w).pin_memory()
+        hout = torch.empty((M, L.H), dtype=torch.int16).pin_memory()
+        host[M] = (hx, hid, hw, hout)
+        h2d += hx.numel() * 2 + hid.numel() * 4 + hw.numel() * 4
+        d2h += hout.numel() * 2
+    e_st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e_st[i].record(stream)
+        for M in wl.Ms:
+            hx, hid, hw, hout = host[M]
+            x, ids, w, out = devb[M]
+            x.view(torch.int16).copy_(hx, non_blocking=True)
+            ids.copy_(hid, non_blocking=True)
+            w.copy_(hw, non_blocking=True)
+            call(M)
+            hout.copy_(out.view(torch.int16), non_blocking=True)
+        e_en[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_st, e_en))
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * tokens_per_step * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        sample = oracle_sample(wl, batches, max_slots=args.cpu_slots)
+        tok, secs = run_oracle(wl, host_w, sample)
+        cpu = {"value": tok / secs, "unit": "tokens/s", "cores": oracle.num_threads(),
+               "kind": "oracle", "sample": describe_sample(sample, wl)}
+
+    pages = [PAGES_MS.get(M) for M in wl.Ms]
+    vs = None
+    if L.E == 384 and all(p is not None for p in pages):
+        vs = value / (tokens_per_step / (sum(pages) / 1e3))
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": vs, "dtype": "f16 MMA operands, f32 accumulate (int4 weights)",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "Ms": list(wl.Ms), "E": L.E, "H": L.H, "I": L.I,
+                       "k": L.k, "group": 32,
+                       "routing": "zipf(1.1)-biased" if wl.zipf_s else "uniform",
+                       "l2": "flushed before every step (write of 2x L2)",
+                       "parallelism": f"replicas x{world}",
+                       "vs_baseline_ref": "pages' sweep on one RTX PRO 6000 (sm_120): context"},
+            "clocks": clocks, "e2e": e2e, "gpu_launches": gpu_launches,
+            "roofline": {"bound": "hbm", "kernel": "gemm_gate_up", "achieved": achieved,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                         "peak_source": f"{peak_kind} hbm_gbs", "traffic": None,
+                         "algorithmic_bytes_per_unit": b13,
+                         "unit_of_work": "active expert (w13 codes + scales)"},
+            "cpu_baseline": cpu, "sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(CONFIGS), default="decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-slots", type=int, default=800,
+                    help="slots the CPU-baseline oracle sample covers")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    wl = CONFIGS[args.config]
+    if args.impl == "reference":
+        return reference_arm(args, wl)
+    return our_arm(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

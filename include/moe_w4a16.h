@@ -1,0 +1,204 @@
+/*
+ * moe_w4a16.h -- C ABI of the GB300 (sm_103a) weight-only-INT4 MoE layer
+ * forward: top-k routed token alignment, grouped gate+up GEMM with a fused
+ * SiLU(gate)*up epilogue, grouped down GEMM, fixed-order top-k combine.
+ *
+ * The operation (page title, section):
+ *  - "The MoE Throughput Lever: Quantifying the INT4 Marlin GEMM on Blackwell
+ *    PRO 6000", "The Benchmark: What Was Measured": an MoE GEMM with INT4
+ *    weights in groups of 32, 16-bit activations, top-8 routing over E=384
+ *    experts, hidden 7168, intermediate 2048, weights repacked once into the
+ *    kernel's own layout before use.
+ *  - "perf(exl3): accelerate fat-expert prefill - #77", "Rollout" and
+ *    "Summary": routed tokens are sorted by expert and each expert's rows run
+ *    as one batch through a stacked gate+up GEMM; results are written back to
+ *    token rows ("direct"/"scatter" writes).
+ *  - "DeepSeek-V4.1-Flash-EXL3 ... Detailed results", "Nsight Compute on the
+ *    stock kernel": the per-expert count scan, serial there, is done here
+ *    with warp shuffles.
+ * Definition used (the pages give no formula):
+ *   W[e][n][kk] = (q - 8) * scale[e][n][kk / 32],  q in [0, 15]
+ *   a = silu(x W13_gate^T) * (x W13_up^T)   with rows [0, I) of w13 = gate
+ *   y = a W2^T,   out[t] = bf16( sum_{j=0..k-1 ascending} topk_w[t][j] * y(t,j) )
+ *
+ * Conventions for every entry point:
+ *  - The caller owns every buffer; the library allocates no device memory.
+ *  - Device pointers must be device-accessible; the library never reads them
+ *    on the host.  Calls taking a stream are asynchronous on that stream
+ *    (except moe_w4a16_prepack and moe_w4a16_get_device_status, which wait).
+ *  - Host-detectable errors (null or misaligned pointers, bad sizes, small
+ *    workspace, no sm_103 device) return before anything is launched.
+ *  - Errors found on the device (an expert id outside [0, E), a prepacked
+ *    buffer whose header does not match, an activation beyond fp16 range,
+ *    a bounded wait that ran out) never trap: the kernels record the first
+ *    one in the workspace's status word and skip the affected work.
+ *    moe_w4a16_get_device_status() reads it back.  Each forward or align
+ *    call resets the word when it starts.
+ *  - A workspace must not be used by two calls that overlap on the GPU.
+ */
+#ifndef MOE_W4A16_H
+#define MOE_W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,          /* null pointer, size out of range */
+    MOE_ERR_MISALIGNED = 2,           /* pointer below its required alignment */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 3,
+    MOE_ERR_BAD_LAYOUT = 4,           /* prepacked header does not match */
+    MOE_ERR_UNSUPPORTED_DEVICE = 5,   /* current device is not sm_103 */
+    MOE_ERR_CUDA = 6,                 /* a CUDA runtime call failed */
+    MOE_ERR_DEVICE_BAD_EXPERT_ID = 7, /* an id outside [0, E) was seen */
+    MOE_ERR_DEVICE_TIMEOUT = 8,       /* a bounded device wait gave up */
+    MOE_ERR_DEVICE_FP16_RANGE = 9     /* a value is not representable in fp16 */
+} moe_status_t;
+
+/* Which matrix a prepacked buffer holds. */
+typedef enum {
+    MOE_PACK_W13 = 1, /* gate+up, canonical [E][2I][H/2]: N = 2I, K = H */
+    MOE_PACK_W2 = 2   /* down,    canonical [E][H][I/2]:  N = H,  K = I */
+} moe_pack_kind_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *moe_status_string(moe_status_t status);
+
+/*
+ * Bytes of the two prepacked buffers for one matrix: the packed codes and
+ * the scales, each with a 256-byte header.  Requires group == 32,
+ * N % 128 == 0, K % 128 == 0, E >= 1; otherwise returns MOE_ERR_INVALID_ARG
+ * and sets both sizes to 0.
+ */
+moe_status_t moe_w4a16_prepack_sizes(int kind, int E, int N, int K, int group,
+                                     size_t *code_bytes, size_t *scale_bytes);
+
+/*
+ * Repack canonical weights into the library's layout (done once per layer at
+ * load time, ahead of any forward).  The weight repack step corresponds to
+ * the repack path the MoE GEMM sweep drives before timing ("The MoE
+ * Throughput Lever", "The Benchmark: What Was Measured").
+ *
+ *  q_canon [E][N][K/2] uint8, device: element kk of row n sits in byte kk/2,
+ *          in the low nibble when kk is even, the high nibble when odd.
+ *  scales  [E][N][K/32] bf16 bit patterns, device.
+ *  code_dst / scale_dst: device buffers of at least the sizes given by
+ *          moe_w4a16_prepack_sizes, 256-byte aligned.
+ * Layout written: per expert, 128-row tiles (for w13 each tile holds 64 gate
+ * rows interleaved with the 64 matching up rows), per 128-element K chunk one
+ * 8 KiB code block and one 1 KiB scale block, codes reordered for a cheap
+ * 4-bit -> fp16 conversion and scales stored as fp16.
+ *
+ * Every scale must be zero, NaN, infinite or of magnitude in
+ * [2^-14, 8188] so that every (q - 8) * scale is exact in fp16; otherwise the
+ * call returns MOE_ERR_DEVICE_FP16_RANGE and marks the buffers invalid.
+ * This call waits for its own work on `stream` to finish.
+ */
+moe_status_t moe_w4a16_prepack(int kind, const uint8_t *q_canon,
+                               const uint16_t *scales, int E, int N, int K,
+                               int group, void *code_dst, size_t code_bytes,
+                               void *scale_dst, size_t scale_bytes,
+                               moe_stream_t stream);
+
+/* Workspace bytes needed by moe_align (256-byte aligned buffer). */
+size_t moe_align_workspace_size(int M, int k, int E);
+
+/*
+ * Top-k routed token alignment (the "sorted routing" stage of
+ * "perf(exl3): accelerate fat-expert prefill - #77", "Rollout"): a stable
+ * counting sort of the M*k flat slot indices f = t*k + j by expert id.
+ *
+ *  topk_ids [M][k] int32, device.
+ *  counts   [E]   int32, device, out: valid slots per expert.
+ *  offsets  [E+1] int32, device, out: exclusive prefix sum of counts.
+ *  perm     [M*k] int32, device, out: perm[offsets[e] + r] = the r-th
+ *           smallest f with topk_ids[f] == e; entries from offsets[E] on are
+ *           set to -1.
+ *  inv_perm [M*k] int32, device, out (may be NULL): position of f in perm,
+ *           or -1 when topk_ids[f] is outside [0, E).
+ * Limits: 1 <= E <= 1024, 1 <= k <= 64, 0 <= M, M*k < 2^31.
+ * Out-of-range ids are left out and reported as MOE_ERR_DEVICE_BAD_EXPERT_ID
+ * through the workspace status word.  M == 0 writes zero counts and offsets.
+ */
+moe_status_t moe_align(const int32_t *topk_ids, int M, int k, int E,
+                       int32_t *counts, int32_t *offsets, int32_t *perm,
+                       int32_t *inv_perm, void *workspace, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/* Workspace bytes needed by moe_w4a16_forward (256-byte aligned buffer). */
+size_t moe_w4a16_workspace_size(int M, int k, int E, int H, int I);
+
+/*
+ * MoE layer forward.
+ *  hidden [M][H] bf16, device, 16-byte aligned.
+ *  topk_ids [M][k] int32, topk_w [M][k] fp32 (used as given), device.
+ *  w13/s13: prepacked gate+up codes/scales (kind MOE_PACK_W13, N = 2I, K = H)
+ *  w2/s2:   prepacked down codes/scales   (kind MOE_PACK_W2,  N = H,  K = I)
+ *  out [M][H] bf16, device, 16-byte aligned: written once, rounded to
+ *           nearest-even from an fp32 combine over ascending slots.
+ *  workspace: moe_w4a16_workspace_size(...) bytes, 256-byte aligned.
+ * Limits: H % 128 == 0, I % 128 == 0, 1 <= E <= 1024, 1 <= k <= 64,
+ * 0 <= M, M*k < 2^31.  M == 0 returns MOE_OK without launching.
+ * Numerics: weights dequantised exactly to fp16, hidden converted to fp16
+ * (values beyond fp16 range set MOE_ERR_DEVICE_FP16_RANGE), fp32
+ * accumulation, the activation passed to the down GEMM as an fp16 hi+lo pair.
+ */
+moe_status_t moe_w4a16_forward(const uint16_t *hidden, const int32_t *topk_ids,
+                               const float *topk_w, const void *w13,
+                               const void *s13, const void *w2, const void *s2,
+                               uint16_t *out, int M, int k, int E, int H, int I,
+                               void *workspace, size_t ws_bytes,
+                               moe_stream_t stream);
+
+/*
+ * Same as moe_w4a16_forward, and additionally records CUDA events around each
+ * kernel it launches, for per-kernel timing.  `events` points to
+ * n_events >= 6 cudaEvent_t handles (created by the caller, timing enabled):
+ * events[i] is recorded right before kernel i and events[5] after the last;
+ * kernel order: 0 align, 1 hidden gather, 2 gate+up GEMM, 3 down GEMM,
+ * 4 combine.  Recording between kernels stops them from overlapping, so the
+ * sum of the intervals can exceed the plain forward's time.  Returns
+ * MOE_ERR_INVALID_ARG if events is NULL or n_events < 6.
+ */
+moe_status_t moe_w4a16_forward_profiled(const uint16_t *hidden, const int32_t *topk_ids,
+                                        const float *topk_w, const void *w13,
+                                        const void *s13, const void *w2, const void *s2,
+                                        uint16_t *out, int M, int k, int E, int H, int I,
+                                        void *workspace, size_t ws_bytes,
+                                        moe_stream_t stream, void **events, int n_events);
+
+/*
+ * Wait for `stream`, then return the status word the device recorded in
+ * `workspace` during the most recent align/forward call on it (MOE_OK if
+ * nothing went wrong).  `detail` (may be NULL) receives a code-specific
+ * value: the offending id, or the kernel that gave up.
+ */
+moe_status_t moe_w4a16_get_device_status(const void *workspace,
+                                         moe_stream_t stream, int32_t *detail);
+
+/* Diagnostics of the most recent forward call issued from this process. */
+typedef struct {
+    int32_t version;          /* 1 */
+    int32_t M, k, E, H, I;
+    int32_t token_tile;       /* token rows per MMA tile (the MMA N extent) */
+    int32_t grid_gemm1;       /* CTAs of the gate+up GEMM */
+    int32_t grid_gemm2;       /* CTAs of the down GEMM */
+    int32_t kernels_launched; /* kernels one forward call launches */
+    int64_t workspace_bytes;  /* bytes of workspace the call used */
+    int64_t calls;            /* forward calls since load */
+} moe_diag_t;
+
+moe_status_t moe_w4a16_get_diag(moe_diag_t *diag);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_W4A16_H */

@@ -1,0 +1,164 @@
+// align.cu -- top-k routed token alignment: per-expert histogram, warp-shuffle
+// prefix scan, stable permutation.
+//
+// "perf(exl3): accelerate fat-expert prefill - #77" ("Rollout") groups routed
+// tokens by expert ("sorted routing"); "DeepSeek-V4.1-Flash-EXL3 ... Detailed
+// results" ("Nsight Compute on the stock kernel") found the serial scan over
+// 384 expert counts to be the hottest spot of decode.  Here the scan is a
+// two-level warp-shuffle scan over one count per thread.
+//
+// One CTA of 1024 threads.  The M*k flat slots are cut into 32 contiguous
+// segments, one per warp.  Each warp builds its segment's histogram with
+// __match_any_sync (no atomics decide any order), the block turns the 32 x E
+// table into per-(warp, expert) starting positions, and each warp walks its
+// segment again in order, so the permutation is the stable counting sort by
+// expert of the flat index f = t*k + j.
+#include "device_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+
+// Exclusive scan of one int per thread over the whole block; returns the
+// thread's exclusive prefix and writes the block total to *total.
+__device__ int block_exclusive_scan(int v, int *warp_buf, int *total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_buf[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int s = warp_buf[lane];
+        int incl = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        warp_buf[lane] = incl - s;
+        if (lane == 31) warp_buf[32] = incl;
+    }
+    __syncthreads();
+    int excl = warp_buf[w] + x - v;
+    *total = warp_buf[32];
+    __syncthreads();
+    return excl;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) align_kernel(AlignArgs a) {
+    extern __shared__ int32_t table[];  // [kWarps][E]
+    __shared__ int warp_buf[33];
+    __shared__ int s_invalid;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int E = a.E, n = a.n;
+
+    if (tid == 0) {
+        a.ctrl->status = 0;
+        a.ctrl->detail = 0;
+        s_invalid = 0;
+    }
+    for (int i = tid; i < kWarps * E; i += kThreads) table[i] = 0;
+    __syncthreads();
+    pdl_trigger();
+
+    const int per = (n + kWarps - 1) / kWarps;
+    const int seg_lo = min(n, w * per), seg_hi = min(n, seg_lo + per);
+    int32_t *row = table + w * E;
+
+    // Phase A: per-warp histogram of its segment.
+    int my_invalid = 0, first_bad = 0;
+    for (int base = seg_lo; base < seg_hi; base += 32) {
+        const int f = base + lane;
+        int id = -1;
+        if (f < seg_hi) {
+            id = __ldg(a.ids + f);
+            if (id < 0 || id >= E) {
+                if (my_invalid == 0) first_bad = id;
+                ++my_invalid;
+                id = -1;
+            }
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, id);
+        if (id >= 0 && lane == __ffs(peers) - 1) row[id] += __popc(peers);
+        __syncwarp();
+    }
+    if (my_invalid) {
+        atomicAdd(&s_invalid, my_invalid);
+        set_status(a.ctrl, MOE_ERR_DEVICE_BAD_EXPERT_ID, first_bad);
+    }
+    __syncthreads();
+
+    // Counts, then the warp-shuffle scan into offsets.
+    int c = 0;
+    if (tid < E) {
+#pragma unroll 8
+        for (int ww = 0; ww < kWarps; ++ww) c += table[ww * E + tid];
+    }
+    int total = 0;
+    const int off = block_exclusive_scan(c, warp_buf, &total);
+    if (tid < E) {
+        a.counts[tid] = c;
+        a.offsets[tid] = off;
+        // Phase B: starting position of (warp, expert) = offsets[e] + the
+        // expert's slots in earlier segments.
+        int run = off;
+        for (int ww = 0; ww < kWarps; ++ww) {
+            int t = table[ww * E + tid];
+            table[ww * E + tid] = run;
+            run += t;
+        }
+    }
+    if (tid == 0) a.offsets[E] = total;
+    if (a.token_tile > 0) {
+        const int tiles = (tid < E) ? (c + a.token_tile - 1) / a.token_tile : 0;
+        int ttotal = 0;
+        const int toff = block_exclusive_scan(tiles, warp_buf, &ttotal);
+        if (tid < E) a.tile_prefix[tid] = toff;
+        if (tid == 0) a.tile_prefix[E] = ttotal;
+    }
+    __syncthreads();
+
+    // Phase C: stable placement, walking each segment in order.
+    for (int base = seg_lo; base < seg_hi; base += 32) {
+        const int f = base + lane;
+        int id = -1;
+        if (f < seg_hi) {
+            id = __ldg(a.ids + f);
+            if (id < 0 || id >= E) id = -1;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, id);
+        int pos = -1;
+        if (id >= 0) pos = row[id] + __popc(peers & ((1u << lane) - 1u));
+        __syncwarp();
+        if (id >= 0 && lane == __ffs(peers) - 1) row[id] += __popc(peers);
+        __syncwarp();
+        if (f < seg_hi) {
+            if (pos >= 0) a.perm[pos] = f;
+            if (a.inv_perm) a.inv_perm[f] = pos;
+        }
+    }
+    __syncthreads();
+    for (int p = total + tid; p < n; p += kThreads) a.perm[p] = -1;
+    if (tid == 0) a.ctrl->n_invalid = s_invalid;
+}
+
+}  // namespace
+
+cudaError_t launch_align(const AlignArgs &a, cudaStream_t s) {
+    // The first kernel of a call: ordinary stream order (no early launch), so
+    // it never overlaps the previous call's kernels on the same workspace.
+    const size_t smem = (size_t)kWarps * a.E * sizeof(int32_t);
+    cudaError_t err = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+    if (err != cudaSuccess) return err;
+    align_kernel<<<1, kThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,320 @@
+// api.cu -- the C ABI: argument validation, workspace carving and the
+// stream-ordered launch sequence of the MoE layer forward.
+#include <climits>
+#include <cstring>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+AlignLayout align_layout(int, int, int) {
+    AlignLayout l;
+    l.ctrl = 0;
+    l.total = sizeof(Ctrl);
+    return l;
+}
+
+FwdLayout fwd_layout(int M, int k, int E, int H, int I) {
+    const size_t n = (size_t)M * k;
+    FwdLayout l;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    l.ctrl = take(sizeof(Ctrl));
+    l.counts = take((size_t)E * 4);
+    l.offsets = take((size_t)(E + 1) * 4);
+    l.tile_prefix = take((size_t)(E + 1) * 4);
+    l.perm = take(n * 4);
+    l.inv_perm = take(n * 4);
+    l.xs = take(n * H * 2);
+    l.act_hi = take(n * I * 2);
+    l.act_lo = take(n * I * 2);
+    l.y = take(n * H * 4);
+    l.total = off;
+    return l;
+}
+
+namespace {
+
+moe_diag_t g_diag = {1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status_t check_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_UNSUPPORTED_DEVICE;
+    }
+    static int verdict[64] = {0};  // 0 unknown, 1 supported, 2 not
+    if (dev >= 0 && dev < 64 && verdict[dev]) return verdict[dev] == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED_DEVICE;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_UNSUPPORTED_DEVICE;
+    }
+    const bool ok = (major == 10 && minor == 3);
+    if (dev >= 0 && dev < 64) verdict[dev] = ok ? 1 : 2;
+    return ok ? MOE_OK : MOE_ERR_UNSUPPORTED_DEVICE;
+}
+
+bool routing_sizes_ok(int M, int k, int E) {
+    return M >= 0 && k >= 1 && k <= 64 && E >= 1 && E <= 1024 && (int64_t)M * k < INT_MAX;
+}
+
+bool layer_sizes_ok(int M, int k, int E, int H, int I) {
+    return routing_sizes_ok(M, k, E) && H > 0 && I > 0 && H % kChunkK == 0 &&
+           I % kChunkK == 0 && H <= (1 << 20) && I <= (1 << 20) &&
+           (int64_t)M * k * H < ((int64_t)1 << 40);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char *moe_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: null pointer or size out of range";
+        case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED: pointer below its required alignment";
+        case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+        case MOE_ERR_BAD_LAYOUT: return "MOE_ERR_BAD_LAYOUT: prepacked buffer header does not match";
+        case MOE_ERR_UNSUPPORTED_DEVICE: return "MOE_ERR_UNSUPPORTED_DEVICE: needs an sm_103 GPU";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA runtime call failed";
+        case MOE_ERR_DEVICE_BAD_EXPERT_ID: return "MOE_ERR_DEVICE_BAD_EXPERT_ID: expert id outside [0, E)";
+        case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
+        case MOE_ERR_DEVICE_FP16_RANGE: return "MOE_ERR_DEVICE_FP16_RANGE: value not representable in fp16";
+    }
+    return "MOE_ERR_UNKNOWN";
+}
+
+moe_status_t moe_w4a16_prepack_sizes(int kind, int E, int N, int K, int group,
+                                     size_t *code_b, size_t *scale_b) {
+    if (code_b) *code_b = 0;
+    if (scale_b) *scale_b = 0;
+    if (!code_b || !scale_b) return MOE_ERR_INVALID_ARG;
+    if ((kind != MOE_PACK_W13 && kind != MOE_PACK_W2) || group != kGroup || E < 1 || N <= 0 ||
+        K <= 0 || N % kTileRows || K % kChunkK || N > (1 << 20) || K > (1 << 20))
+        return MOE_ERR_INVALID_ARG;
+    *code_b = code_bytes(E, N, K);
+    *scale_b = scale_bytes(E, N, K);
+    return MOE_OK;
+}
+
+moe_status_t moe_w4a16_prepack(int kind, const uint8_t *q_canon, const uint16_t *scales, int E,
+                               int N, int K, int group, void *code_dst, size_t code_b,
+                               void *scale_dst, size_t scale_b, moe_stream_t stream) {
+    size_t need_c = 0, need_s = 0;
+    moe_status_t st = moe_w4a16_prepack_sizes(kind, E, N, K, group, &need_c, &need_s);
+    if (st != MOE_OK) return st;
+    if (!q_canon || !scales || !code_dst || !scale_dst) return MOE_ERR_INVALID_ARG;
+    if (!aligned(q_canon, 16) || !aligned(scales, 16) || !aligned(code_dst, 256) ||
+        !aligned(scale_dst, 256))
+        return MOE_ERR_MISALIGNED;
+    if (code_b < need_c || scale_b < need_s) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if ((st = check_device()) != MOE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    PackHeader hc;
+    std::memset(&hc, 0, sizeof hc);
+    hc.magic = kPackMagic;
+    hc.version = kPackVersion;
+    hc.kind = (uint32_t)kind;
+    hc.part = kPartCodes;
+    hc.E = E;
+    hc.N = N;
+    hc.K = K;
+    hc.group = group;
+    hc.status = MOE_OK;
+    PackHeader hs = hc;
+    hs.part = kPartScales;
+    uint8_t *cd = static_cast<uint8_t *>(code_dst), *sd = static_cast<uint8_t *>(scale_dst);
+    int32_t *flag = &reinterpret_cast<PackHeader *>(sd)->status;
+    if (cudaMemcpyAsync(cd, &hc, sizeof hc, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(sd, &hs, sizeof hs, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        launch_prepack_codes(kind, q_canon, E, N, K, cd, s) != cudaSuccess ||
+        launch_prepack_scales(kind, scales, E, N, K, sd, flag, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    int32_t dev_status = 0;
+    if (cudaMemcpy(&dev_status, flag, sizeof dev_status, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return dev_status == MOE_OK ? MOE_OK : MOE_ERR_DEVICE_FP16_RANGE;
+}
+
+size_t moe_align_workspace_size(int M, int k, int E) {
+    if (!routing_sizes_ok(M, k, E)) return 0;
+    return align_layout(M, k, E).total;
+}
+
+moe_status_t moe_align(const int32_t *ids, int M, int k, int E, int32_t *counts, int32_t *offsets,
+                       int32_t *perm, int32_t *inv_perm, void *workspace, size_t ws_bytes,
+                       moe_stream_t stream) {
+    if (!routing_sizes_ok(M, k, E)) return MOE_ERR_INVALID_ARG;
+    if (!counts || !offsets || !workspace || (M > 0 && (!ids || !perm))) return MOE_ERR_INVALID_ARG;
+    if (!aligned(ids, 4) || !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(perm, 4) ||
+        !aligned(inv_perm, 4) || !aligned(workspace, 256))
+        return MOE_ERR_MISALIGNED;
+    if (ws_bytes < align_layout(M, k, E).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    moe_status_t st = check_device();
+    if (st != MOE_OK) return st;
+    AlignArgs a = {};
+    a.ids = ids;
+    a.n = M * k;
+    a.E = E;
+    a.token_tile = 0;
+    a.counts = counts;
+    a.offsets = offsets;
+    a.perm = perm;
+    a.inv_perm = inv_perm;
+    a.tile_prefix = nullptr;
+    a.ctrl = reinterpret_cast<Ctrl *>(static_cast<uint8_t *>(workspace) + align_layout(M, k, E).ctrl);
+    if (launch_align(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+size_t moe_w4a16_workspace_size(int M, int k, int E, int H, int I) {
+    if (!layer_sizes_ok(M, k, E, H, I)) return 0;
+    return fwd_layout(M, k, E, H, I).total;
+}
+
+static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, const float *topk_w,
+                                 const void *w13, const void *s13, const void *w2, const void *s2,
+                                 uint16_t *out, int M, int k, int E, int H, int I, void *workspace,
+                                 size_t ws_bytes, moe_stream_t stream, cudaEvent_t *ev) {
+    if (!layer_sizes_ok(M, k, E, H, I)) return MOE_ERR_INVALID_ARG;
+    if (!w13 || !s13 || !w2 || !s2 || !workspace) return MOE_ERR_INVALID_ARG;
+    if (M > 0 && (!hidden || !ids || !topk_w || !out)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(hidden, 16) || !aligned(out, 16) || !aligned(ids, 4) || !aligned(topk_w, 4) ||
+        !aligned(w13, 256) || !aligned(s13, 256) || !aligned(w2, 256) || !aligned(s2, 256) ||
+        !aligned(workspace, 256))
+        return MOE_ERR_MISALIGNED;
+    const FwdLayout L = fwd_layout(M, k, E, H, I);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    moe_status_t st = check_device();
+    if (st != MOE_OK) return st;
+    if (M == 0) return MOE_OK;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(ws + L.ctrl);
+    int32_t *counts = reinterpret_cast<int32_t *>(ws + L.counts);
+    int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    int32_t *tile_prefix = reinterpret_cast<int32_t *>(ws + L.tile_prefix);
+    int32_t *perm = reinterpret_cast<int32_t *>(ws + L.perm);
+    int32_t *inv_perm = reinterpret_cast<int32_t *>(ws + L.inv_perm);
+    uint16_t *xs = reinterpret_cast<uint16_t *>(ws + L.xs);
+    uint16_t *act_hi = reinterpret_cast<uint16_t *>(ws + L.act_hi);
+    uint16_t *act_lo = reinterpret_cast<uint16_t *>(ws + L.act_lo);
+    float *y = reinterpret_cast<float *>(ws + L.y);
+    const int n = M * k;
+    const int tile = simple_token_tile();
+
+    AlignArgs al = {ids, n, E, tile, counts, offsets, perm, inv_perm, tile_prefix, ctrl};
+    GatherArgs ga = {hidden, perm, offsets, n, k, H, E, xs, ctrl};
+    GemmArgs g1 = {};
+    g1.w_codes = static_cast<const uint8_t *>(w13);
+    g1.w_scales = static_cast<const uint8_t *>(s13);
+    g1.offsets = offsets;
+    g1.n = n;
+    g1.E = E;
+    g1.N = 2 * I;
+    g1.K = H;
+    g1.I = I;
+    g1.kind = MOE_PACK_W13;
+    g1.in_hi = xs;
+    g1.act_hi = act_hi;
+    g1.act_lo = act_lo;
+    g1.ctrl = ctrl;
+    GemmArgs g2 = g1;
+    g2.w_codes = static_cast<const uint8_t *>(w2);
+    g2.w_scales = static_cast<const uint8_t *>(s2);
+    g2.N = H;
+    g2.K = I;
+    g2.kind = MOE_PACK_W2;
+    g2.in_hi = act_hi;
+    g2.in_lo = act_lo;
+    g2.y = y;
+    CombineArgs cb = {y, inv_perm, topk_w, M, k, H, out};
+
+    auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
+    const bool pdl = (ev == nullptr);
+    if (mark(0) != cudaSuccess || launch_align(al, s) != cudaSuccess || mark(1) != cudaSuccess ||
+        launch_gather_hidden(ga, s, pdl) != cudaSuccess || mark(2) != cudaSuccess ||
+        launch_gemm_simple(g1, tile_prefix, s, pdl) != cudaSuccess || mark(3) != cudaSuccess ||
+        launch_gemm_simple(g2, tile_prefix, s, pdl) != cudaSuccess || mark(4) != cudaSuccess ||
+        launch_combine(cb, s, pdl) != cudaSuccess || mark(5) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    g_diag.M = M;
+    g_diag.k = k;
+    g_diag.E = E;
+    g_diag.H = H;
+    g_diag.I = I;
+    g_diag.token_tile = tile;
+    g_diag.grid_gemm1 = 0;
+    g_diag.grid_gemm2 = 0;
+    g_diag.kernels_launched = 5;
+    g_diag.workspace_bytes = (int64_t)L.total;
+    g_diag.calls += 1;
+    return MOE_OK;
+}
+
+moe_status_t moe_w4a16_forward(const uint16_t *hidden, const int32_t *ids, const float *topk_w,
+                               const void *w13, const void *s13, const void *w2, const void *s2,
+                               uint16_t *out, int M, int k, int E, int H, int I, void *workspace,
+                               size_t ws_bytes, moe_stream_t stream) {
+    return forward_impl(hidden, ids, topk_w, w13, s13, w2, s2, out, M, k, E, H, I, workspace,
+                        ws_bytes, stream, nullptr);
+}
+
+moe_status_t moe_w4a16_forward_profiled(const uint16_t *hidden, const int32_t *ids,
+                                        const float *topk_w, const void *w13, const void *s13,
+                                        const void *w2, const void *s2, uint16_t *out, int M,
+                                        int k, int E, int H, int I, void *workspace,
+                                        size_t ws_bytes, moe_stream_t stream, void **events,
+                                        int n_events) {
+    if (!events || n_events < 6) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 6; ++i)
+        if (!events[i]) return MOE_ERR_INVALID_ARG;
+    return forward_impl(hidden, ids, topk_w, w13, s13, w2, s2, out, M, k, E, H, I, workspace,
+                        ws_bytes, stream, reinterpret_cast<cudaEvent_t *>(events));
+}
+
+moe_status_t moe_w4a16_get_device_status(const void *workspace, moe_stream_t stream,
+                                         int32_t *detail) {
+    if (detail) *detail = 0;
+    if (!workspace) return MOE_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return MOE_ERR_MISALIGNED;
+    Ctrl c;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess ||
+        cudaMemcpy(&c, workspace, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    if (detail) *detail = c.detail;
+    return static_cast<moe_status_t>(c.status);
+}
+
+moe_status_t moe_w4a16_get_diag(moe_diag_t *diag) {
+    if (!diag) return MOE_ERR_INVALID_ARG;
+    *diag = g_diag;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,104 @@
+// elementwise.cu -- the two HBM-bound row kernels around the expert GEMMs:
+//   gather_hidden: xs[p] = fp16(hidden[perm[p] / k]), the hidden rows in
+//                  expert-sorted order as the gate+up GEMM's token operand;
+//   combine:       out[t] = bf16(sum_{j ascending} topk_w[t][j] * y[inv_perm[t*k+j]]),
+//                  the fixed-order top-k combine back to token rows (the
+//                  "direct/scatter" row writes of "perf(exl3): accelerate
+//                  fat-expert prefill - #77", "Engagement and fallback proof").
+#include "device_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+
+// One warp per sorted row; 16-byte loads and stores (8 elements per lane).
+__global__ void __launch_bounds__(kThreads) gather_hidden_kernel(GatherArgs a) {
+    pdl_wait();
+    pdl_trigger();
+    const int valid = __ldg(a.offsets + a.E);
+    const int warps = kThreads / 32;
+    const int lane = threadIdx.x & 31;
+    const int vecs = a.H / 8;
+    bool overflow = false;
+    for (int p = blockIdx.x * warps + (threadIdx.x >> 5); p < valid; p += gridDim.x * warps) {
+        const int t = __ldg(a.perm + p) / a.k;
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.hidden + (size_t)t * a.H);
+        uint4 *dst = reinterpret_cast<uint4 *>(a.xs + (size_t)p * a.H);
+        for (int v = lane; v < vecs; v += 32) {
+            const uint4 in = __ldg(src + v);
+            const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float lo = __uint_as_float(w[i] << 16);
+                const float hi = __uint_as_float(w[i] & 0xFFFF0000u);
+                overflow |= (fabsf(lo) > 65504.0f && !isinf(lo)) || (fabsf(hi) > 65504.0f && !isinf(hi));
+                const __half2 h = __floats2half2_rn(lo, hi);
+                o[i] = *reinterpret_cast<const uint32_t *>(&h);
+            }
+            dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    if (overflow) set_status(a.ctrl, MOE_ERR_DEVICE_FP16_RANGE, 0);
+}
+
+// One thread per 4 consecutive outputs of one token row.
+__global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
+    pdl_wait();
+    pdl_trigger();
+    const int quads = a.H / 4;
+    const int64_t total = (int64_t)a.M * quads;
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * kThreads) {
+        const int t = (int)(i / quads), q = (int)(i % quads);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < a.k; ++j) {
+            const int pos = __ldg(a.inv_perm + (size_t)t * a.k + j);
+            if (pos < 0) continue;
+            const float w = __ldg(a.topk_w + (size_t)t * a.k + j);
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(a.y + (size_t)pos * a.H) + q);
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+        }
+        const __nv_bfloat162 b01 = __floats2bfloat162_rn(acc.x, acc.y);
+        const __nv_bfloat162 b23 = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 o;
+        o.x = *reinterpret_cast<const uint32_t *>(&b01);
+        o.y = *reinterpret_cast<const uint32_t *>(&b23);
+        reinterpret_cast<uint2 *>(a.out + (size_t)t * a.H)[q] = o;
+    }
+}
+
+template <typename Kernel, typename Args>
+cudaError_t launch(Kernel k, const Args &args, int blocks, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks > 0 ? blocks : 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, args);
+}
+
+}  // namespace
+
+cudaError_t launch_gather_hidden(const GatherArgs &a, cudaStream_t s, bool pdl) {
+    const int warps = kThreads / 32;
+    int64_t blocks = ((int64_t)a.n + warps - 1) / warps;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    return launch(gather_hidden_kernel, a, (int)blocks, s, pdl);
+}
+
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s, bool pdl) {
+    int64_t blocks = ((int64_t)a.M * (a.H / 4) + kThreads - 1) / kThreads;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    return launch(combine_kernel, a, (int)blocks, s, pdl);
+}
+
+}  // namespace moe

@@ -1,0 +1,141 @@
+// moe_internal.h -- layouts and launchers shared by the library's .cu files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "moe_w4a16.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Prepacked weight layout.
+//
+// Every prepacked buffer starts with a 256-byte header, then blocks.  A block
+// covers one 128-row tile of one expert and one 128-element K chunk:
+//   code block  (8192 B): 4 pieces x 128 rows x 16 B; piece pc of row r at
+//                         byte (pc*128 + r)*16 holds K elements
+//                         [32pc, 32pc+32) of the chunk as 4 words; word w
+//                         covers elements 8w..8w+7 with nibbles, low to high,
+//                         in element order 0,2,4,6,1,3,5,7.
+//   scale block (1024 B): 128 rows x 4 groups of fp16, row r group g at
+//                         byte (r*4 + g)*2.
+// Block index = (e * tiles_per_expert + tile) * k_chunks + chunk.
+// For w13, tile t holds gate rows 64t..64t+63 at even tile rows (row 2j =
+// gate row 64t+j) and the matching up rows at odd tile rows (2j+1).
+// ---------------------------------------------------------------------------
+constexpr int kTileRows = 128;
+constexpr int kChunkK = 128;
+constexpr int kGroup = 32;
+constexpr int kCodeBlockBytes = kTileRows * kChunkK / 2;       // 8192
+constexpr int kScaleBlockBytes = kTileRows * (kChunkK / kGroup) * 2;  // 1024
+constexpr int kHeaderBytes = 256;
+
+constexpr uint32_t kPackMagic = 0x5034574Du;  // "MW4P"
+constexpr uint32_t kPackVersion = 1;
+constexpr uint32_t kPartCodes = 1, kPartScales = 2;
+
+struct PackHeader {
+    uint32_t magic;
+    uint32_t version;
+    uint32_t kind;    // MOE_PACK_W13 / MOE_PACK_W2
+    uint32_t part;    // kPartCodes / kPartScales
+    int32_t E, N, K, group;
+    int32_t status;   // MOE_OK once the prepack finished and validated
+    int32_t pad[3];
+};
+static_assert(sizeof(PackHeader) <= kHeaderBytes, "header too large");
+
+inline size_t code_bytes(int E, int N, int K) {
+    return kHeaderBytes + (size_t)E * (N / kTileRows) * (K / kChunkK) * kCodeBlockBytes;
+}
+inline size_t scale_bytes(int E, int N, int K) {
+    return kHeaderBytes + (size_t)E * (N / kTileRows) * (K / kChunkK) * kScaleBlockBytes;
+}
+
+// ---------------------------------------------------------------------------
+// Workspace control block (first 256 bytes of every workspace).
+// ---------------------------------------------------------------------------
+struct Ctrl {
+    int32_t status;   // first device-side error of the current call
+    int32_t detail;
+    int32_t n_invalid;  // slots whose id was out of range
+    int32_t pad[61];
+};
+static_assert(sizeof(Ctrl) == 256, "ctrl block is 256 bytes");
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Carving of the align workspace.
+struct AlignLayout {
+    size_t ctrl, total;
+};
+AlignLayout align_layout(int M, int k, int E);
+
+// Carving of the forward workspace.
+struct FwdLayout {
+    size_t ctrl, counts, offsets, tile_prefix, perm, inv_perm;
+    size_t xs;          // [n][H] fp16 hidden rows in sorted order
+    size_t act_hi;      // [n][I] fp16
+    size_t act_lo;      // [n][I] fp16
+    size_t y;           // [n][H] fp32
+    size_t total;
+};
+FwdLayout fwd_layout(int M, int k, int E, int H, int I);
+
+// ---------------------------------------------------------------------------
+// Launchers (each returns the cudaError_t of its launch).
+// ---------------------------------------------------------------------------
+struct AlignArgs {
+    const int32_t *ids;
+    int n;            // M * k
+    int E;
+    int token_tile;   // >0: also write tile_prefix for this tile width
+    int32_t *counts, *offsets, *perm, *inv_perm, *tile_prefix;
+    Ctrl *ctrl;
+};
+cudaError_t launch_align(const AlignArgs &a, cudaStream_t s);
+
+cudaError_t launch_prepack_codes(int kind, const uint8_t *q, int E, int N, int K,
+                                 uint8_t *dst, cudaStream_t s);
+cudaError_t launch_prepack_scales(int kind, const uint16_t *sc, int E, int N, int K,
+                                  uint8_t *dst, int32_t *bad_flag, cudaStream_t s);
+
+struct GatherArgs {
+    const uint16_t *hidden;  // [M][H] bf16
+    const int32_t *perm;     // [n]
+    const int32_t *offsets;  // [E+1]; offsets[E] = valid rows
+    int n, k, H, E;
+    uint16_t *xs;            // [n][H] fp16
+    Ctrl *ctrl;
+};
+cudaError_t launch_gather_hidden(const GatherArgs &a, cudaStream_t s, bool pdl);
+
+struct GemmArgs {
+    const uint8_t *w_codes;   // prepacked buffer (header included)
+    const uint8_t *w_scales;
+    const int32_t *offsets;   // [E+1]
+    int n, E, N, K, I;        // N, K of this matrix; I for the w13 epilogue
+    int kind;                 // MOE_PACK_W13 or MOE_PACK_W2
+    const uint16_t *in_hi;    // [n][K] fp16 operand rows (sorted order)
+    const uint16_t *in_lo;    // [n][K] fp16 low parts (w2 only) or null
+    uint16_t *act_hi, *act_lo;  // w13 output [n][I]
+    float *y;                 // w2 output [n][N]
+    Ctrl *ctrl;
+};
+cudaError_t launch_gemm_simple(const GemmArgs &a, const int32_t *tile_prefix, cudaStream_t s,
+                               bool pdl);
+int simple_token_tile();
+
+struct CombineArgs {
+    const float *y;           // [n][H]
+    const int32_t *inv_perm;  // [M*k]
+    const float *topk_w;      // [M][k]
+    int M, k, H;
+    uint16_t *out;            // [M][H] bf16
+};
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s, bool pdl);
+
+}  // namespace moe

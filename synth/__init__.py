@@ -14,9 +14,9 @@ tag, index])))``):
   routing  top-k by descending logit (lower expert index first on ties);
            weights = softmax over the k selected logits (the renormalised
            softmax top-k), computed in fp64 and stored as fp32
-  w13/w2   canonical packed codes [E][N][K/2] uint8, each nibble uniform on
-           {0..15}; element kk of a row sits in byte kk/2, low nibble when kk
-           is even
+  w13/w2   canonical packed codes [E][N][K/2] uint8 taken from the raw 64-bit
+           PCG64 output, so each nibble is uniform on {0..15}; element kk of a
+           row sits in byte kk/2, low nibble when kk is even
   s13/s2   [E][N][K/32] bf16 uniform on [0.002, 0.02]
 
 The workloads are those of the MoE GEMM sweep in "The MoE Throughput Lever:
@@ -109,9 +109,11 @@ def routing(M: int, layer: Layer, seed: int = 0, zipf_s: Optional[float] = None)
 
 
 def packed_codes(N: int, K: int, seed: int, tag: int, e: int) -> np.ndarray:
-    """[N][K/2] uint8: two uniform 4-bit codes per byte."""
-    g = _rng(seed, tag, e)
-    return np.frombuffer(g.bytes(N * (K // 2)), dtype=np.uint8).reshape(N, K // 2).copy()
+    """[N][K/2] uint8: two uniform 4-bit codes per byte (raw PCG64 output)."""
+    nbytes = N * (K // 2)
+    assert nbytes % 8 == 0
+    bg = np.random.PCG64(np.random.SeedSequence([seed, tag, e]))
+    return bg.random_raw(nbytes // 8).view(np.uint8).reshape(N, K // 2)
 
 
 def scales(N: int, K: int, seed: int, tag: int, e: int) -> np.ndarray:
@@ -132,13 +134,21 @@ def layer_weights(layer: Layer, seed: int = 0, experts: Optional[Sequence[int]] 
     """Full canonical arrays [E][...] for every expert.  When ``experts`` is
     given, only those experts are drawn and the others are left zero (codes
     0 and scale 0), which is enough for an oracle restricted to them."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+
     E, H, I = layer.E, layer.H, layer.I
     w13 = np.zeros((E, 2 * I, H // 2), np.uint8)
     s13 = np.zeros((E, 2 * I, H // GROUP), np.uint16)
     w2 = np.zeros((E, H, I // 2), np.uint8)
     s2 = np.zeros((E, H, I // GROUP), np.uint16)
-    for e in (range(E) if experts is None else experts):
+
+    def fill(e):
         w13[e], s13[e], w2[e], s2[e] = expert_weights(layer, int(e), seed)
+
+    todo = list(range(E) if experts is None else experts)
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        list(ex.map(fill, todo))
     return w13, s13, w2, s2
 
 

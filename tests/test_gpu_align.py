@@ -1,0 +1,68 @@
+"""GPU alignment (moe_align) against the oracle: bit-exact counts, offsets,
+permutation and inverse permutation on every workload's routing, plus edge
+cases (M = 0, one slot, duplicate ids, out-of-range ids, all slots on one
+expert)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(ids, E):
+    import torch
+    import quantized_moe_expert_align_gb300 as moe
+    idd = torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int32)).cuda()
+    counts, offsets, perm, inv_perm, ws = moe.align(idd, E)
+    st, detail = moe.moe_w4a16_get_device_status(ws)
+    return (counts.cpu().numpy(), offsets.cpu().numpy(), perm.cpu().numpy(),
+            inv_perm.cpu().numpy(), st, detail)
+
+
+def _check(ids, E):
+    c, o, p, ip, st, detail = _run(ids, E)
+    rc, ro, rp, rip, bad = oracle.align(ids, E)
+    assert np.array_equal(c, rc), "counts"
+    assert np.array_equal(o, ro), "offsets"
+    n = ro[E]
+    assert np.array_equal(p[:n], rp[:n]), "perm"
+    assert np.all(p[n:] == -1), "perm tail"
+    assert np.array_equal(ip, rip), "inv_perm"
+    return st, detail, bad
+
+
+CASES = [(w.name, M) for w in synth.WORKLOADS.values() for M in w.Ms]
+
+
+@pytest.mark.parametrize("name,M", CASES, ids=[f"{n}-M{m}" for n, m in CASES])
+def test_align_bit_exact(gpu, name, M):
+    import quantized_moe_expert_align_gb300 as moe
+    wl = synth.WORKLOADS[name]
+    ids, _ = synth.routing(M, wl.layer, seed=0, zipf_s=wl.zipf_s)
+    st, _, bad = _check(ids, wl.layer.E)
+    assert st == moe.MOE_OK and bad == 0
+
+
+def test_align_edge_cases(gpu):
+    import quantized_moe_expert_align_gb300 as moe
+    rng = np.random.default_rng(0)
+    # one slot; every slot on one expert; duplicates; E = 1; E = 1024
+    for ids, E in [(np.array([[5]]), 8), (np.full((300, 8), 3), 384),
+                   (rng.integers(0, 4, size=(77, 6)), 4), (np.zeros((50, 2)), 1),
+                   (rng.integers(0, 1024, size=(999, 8)), 1024),
+                   (rng.integers(0, 384, size=(16384, 8)), 384)]:
+        st, _, bad = _check(np.asarray(ids, np.int32), E)
+        assert st == moe.MOE_OK and bad == 0
+    # M = 0 writes zero counts/offsets
+    c, o, p, ip, st, _ = _run(np.zeros((0, 8), np.int32), 16)
+    assert np.all(c == 0) and np.all(o == 0) and st == moe.MOE_OK
+
+
+def test_align_out_of_range_ids(gpu):
+    import quantized_moe_expert_align_gb300 as moe
+    ids = np.array([[0, 4], [-1, 2], [2, 0], [3, 1 << 30]], np.int32)
+    st, detail, bad = _check(ids, 4)
+    assert bad == 3
+    assert st == moe.MOE_ERR_DEVICE_BAD_EXPERT_ID and detail in (4, -1, 1 << 30)

@@ -1,0 +1,74 @@
+"""Device-side error reporting: out-of-range expert ids, mismatched prepacked
+buffers, fp16 range; and M = 0.  None of these faults or traps the GPU: the
+kernels record a status word and skip the affected work."""
+import numpy as np
+import pytest
+
+import synth
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def test_invalid_ids_contribute_zero(toy_layer):
+    import quantized_moe_expert_align_gb300 as moe
+    L = synth.TOY.layer
+    x = synth.hidden(3, L.H, seed=2)
+    ids = np.array([[0, 9], [-3, 2], [1, 3]], np.int32)
+    w = np.full((3, 2), 0.5, np.float32)
+    out, ws = toy_layer.forward(x, ids, w)
+    st, detail = moe.moe_w4a16_get_device_status(ws.buf)
+    assert st == moe.MOE_ERR_DEVICE_BAD_EXPERT_ID and detail in (9, -3)
+    gu.parity(gu.bf16_dev_to_f64(out), toy_layer.oracle(x, ids, w), "invalid ids")
+    # the next clean call on the same workspace reports OK again
+    ids2 = np.array([[0, 1], [2, 3], [4, 5]], np.int32)
+    out, ws = toy_layer.forward(x, ids2, w, workspace=ws)
+    assert moe.moe_w4a16_get_device_status(ws.buf)[0] == moe.MOE_OK
+
+
+def test_swapped_buffers_report_bad_layout(toy_layer):
+    import torch
+    import quantized_moe_expert_align_gb300 as moe
+    L = synth.TOY.layer
+    x = gu.to_dev(synth.hidden(4, L.H).view(np.int16)).view(torch.bfloat16)
+    ids, w = synth.routing(4, L)
+    ws = moe.Workspace(4, L.k, L.E, L.H, L.I, "cuda")
+    p13, p2 = toy_layer.p13, toy_layer.p2
+    moe.forward(x, gu.to_dev(ids), gu.to_dev(w), p2[0], p2[1], p13[0], p13[1], L.E, L.I,
+                workspace=ws)
+    assert moe.moe_w4a16_get_device_status(ws.buf)[0] == moe.MOE_ERR_BAD_LAYOUT
+
+
+def test_hidden_beyond_fp16_range(toy_layer):
+    import quantized_moe_expert_align_gb300 as moe
+    L = synth.TOY.layer
+    x = synth.hidden(4, L.H)
+    x[1, 7] = synth.f32_to_bf16_bits(np.array([1.0e5], np.float32))[0]
+    ids, w = synth.routing(4, L)
+    _, ws = toy_layer.forward(x, ids, w)
+    assert moe.moe_w4a16_get_device_status(ws.buf)[0] == moe.MOE_ERR_DEVICE_FP16_RANGE
+
+
+def test_prepack_rejects_scales_outside_fp16(gpu):
+    import quantized_moe_expert_align_gb300 as moe
+    L = synth.TOY.layer
+    w13, s13, _, _ = synth.layer_weights(L)
+    s13 = s13.copy()
+    s13[2, 5, 1] = synth.f32_to_bf16_bits(np.array([1.0e-6], np.float32))[0]
+    with pytest.raises(moe.MoeError) as ei:
+        moe.prepack(moe.MOE_PACK_W13, gu.to_dev(w13), gu.to_dev(s13.view(np.int16)))
+    assert ei.value.status == moe.MOE_ERR_DEVICE_FP16_RANGE
+
+
+def test_m_zero_is_a_noop(toy_layer):
+    import torch
+    import quantized_moe_expert_align_gb300 as moe
+    L = synth.TOY.layer
+    ws = moe.Workspace(1, L.k, L.E, L.H, L.I, "cuda")
+    out = torch.full((0, L.H), 1.0, dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((0, L.H), dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros((0, L.k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((0, L.k), dtype=torch.float32, device="cuda")
+    moe.forward(x, ids, w, toy_layer.p13[0], toy_layer.p13[1], toy_layer.p2[0], toy_layer.p2[1],
+                L.E, L.I, out=out, workspace=ws)
+    torch.cuda.synchronize()
