@@ -146,6 +146,10 @@ size_t moe_w4a16_workspace_size(int M, int k, int E, int H, int I);
  *  workspace: moe_w4a16_workspace_size(...) bytes, 256-byte aligned.
  * Limits: H % 128 == 0, I % 128 == 0, 1 <= E <= 1024, 1 <= k <= 64,
  * 0 <= M, M*k < 2^31.  M == 0 returns MOE_OK without launching.
+ * The token-tile width (rows of expert-sorted tokens per tensor-core tile) is
+ * chosen from M*k/E; for testing, the environment variable
+ * MOE_W4A16_TOKEN_TILE = 16, 32, 64 or 128 fixes it (read once per process;
+ * the workspace size follows it).
  * Numerics: weights dequantised exactly to fp16, hidden converted to fp16
  * (values beyond fp16 range set MOE_ERR_DEVICE_FP16_RANGE), fp32
  * accumulation, the activation passed to the down GEMM as an fp16 hi+lo pair.
@@ -182,6 +186,24 @@ moe_status_t moe_w4a16_forward_profiled(const uint16_t *hidden, const int32_t *t
  */
 moe_status_t moe_w4a16_get_device_status(const void *workspace,
                                          moe_stream_t stream, int32_t *detail);
+
+/*
+ * Where a forward call leaves its intermediates inside the workspace (byte
+ * offsets from the workspace start), for inspection after the call has
+ * completed and before the next call on the same workspace:
+ *   counts [E], offsets [E+1], perm [M*k], inv_perm [M*k]: int32 alignment
+ *   act_hi, act_lo [M*k][I] fp16: a = silu(gate)*up in expert-sorted row
+ *                  order, as the pair hi + lo (hi = fp16(a), lo = fp16(a - hi))
+ *   y [M*k][H] fp32: the down projection of every sorted row.
+ * Rows at and beyond offsets[E] are not written.  Returns
+ * MOE_ERR_INVALID_ARG for sizes moe_w4a16_workspace_size rejects.
+ */
+typedef struct {
+    size_t counts, offsets, perm, inv_perm, act_hi, act_lo, y;
+} moe_ws_views_t;
+
+moe_status_t moe_w4a16_workspace_views(int M, int k, int E, int H, int I,
+                                       moe_ws_views_t *views);
 
 /* Diagnostics of the most recent forward call issued from this process. */
 typedef struct {

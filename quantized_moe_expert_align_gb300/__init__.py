@@ -38,6 +38,11 @@ class MoeError(RuntimeError):
         self.status = status
 
 
+class moe_ws_views_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("counts", "offsets", "perm", "inv_perm", "act_hi", "act_lo", "y")]
+
+
 class moe_diag_t(ctypes.Structure):
     _fields_ = [("version", ctypes.c_int32), ("M", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
@@ -72,6 +77,7 @@ def load(path: str = LIB_PATH):
                                                ctypes.POINTER(p), i]),
             "moe_w4a16_get_device_status": (i, [p, p, ctypes.POINTER(ctypes.c_int32)]),
             "moe_w4a16_get_diag": (i, [ctypes.POINTER(moe_diag_t)]),
+            "moe_w4a16_workspace_views": (i, [i, i, i, i, i, ctypes.POINTER(moe_ws_views_t)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -151,6 +157,39 @@ def moe_w4a16_get_device_status(workspace, stream=None):
     d = ctypes.c_int32(0)
     st = load().moe_w4a16_get_device_status(_p(workspace), _stream(stream), ctypes.byref(d))
     return st, d.value
+
+
+def moe_w4a16_workspace_views(M, k, E, H, I):
+    v = moe_ws_views_t()
+    st = load().moe_w4a16_workspace_views(M, k, E, H, I, ctypes.byref(v))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_w4a16_workspace_views")
+    return {name: getattr(v, name) for name, _ in moe_ws_views_t._fields_}
+
+
+def intermediates(workspace, M, k, E, H, I):
+    """Copies of the sorted intermediates a finished forward left in its
+    workspace: dict of numpy arrays (counts, offsets, perm, inv_perm,
+    act = hi + lo as float64 [valid][I], y [valid][H])."""
+    import numpy as np
+    import torch
+    ws = workspace.buf if isinstance(workspace, Workspace) else workspace
+    v = moe_w4a16_workspace_views(M, k, E, H, I)
+    n = M * k
+
+    def view(off, count, dtype):
+        nbytes = count * torch.empty((), dtype=dtype).element_size()
+        return ws[off:off + nbytes].view(dtype).cpu().numpy()
+
+    torch.cuda.synchronize()
+    offsets = view(v["offsets"], E + 1, torch.int32)
+    valid = int(offsets[E])
+    hi = view(v["act_hi"], n * I, torch.float16).reshape(n, I)[:valid].astype(np.float64)
+    lo = view(v["act_lo"], n * I, torch.float16).reshape(n, I)[:valid].astype(np.float64)
+    return {"counts": view(v["counts"], E, torch.int32), "offsets": offsets,
+            "perm": view(v["perm"], n, torch.int32), "inv_perm": view(v["inv_perm"], n, torch.int32),
+            "act": hi + lo, "act_hi": hi,
+            "y": view(v["y"], n * H, torch.float32).reshape(n, H)[:valid].astype(np.float64)}
 
 
 def moe_w4a16_get_diag():

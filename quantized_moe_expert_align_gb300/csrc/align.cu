@@ -121,6 +121,10 @@ __global__ void __launch_bounds__(kThreads, 1) align_kernel(AlignArgs a) {
         const int toff = block_exclusive_scan(tiles, warp_buf, &ttotal);
         if (tid < E) a.tile_prefix[tid] = toff;
         if (tid == 0) a.tile_prefix[E] = ttotal;
+        if (a.tickets) {
+            for (int i = tid; i < ttotal * a.r1; i += kThreads) a.tickets[i] = 0;
+            for (int i = tid; i < ttotal * a.r2; i += kThreads) a.tickets[a.off2 + i] = 0;
+        }
     }
     __syncthreads();
 

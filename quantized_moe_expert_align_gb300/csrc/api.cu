@@ -1,11 +1,31 @@
 // api.cu -- the C ABI: argument validation, workspace carving and the
 // stream-ordered launch sequence of the MoE layer forward.
 #include <climits>
+#include <cstdlib>
 #include <cstring>
 
+#include "gemm_tc.h"
 #include "moe_internal.h"
 
 namespace moe {
+
+constexpr int kMaxGrid = 256;  // bound on the GEMM grid used to size workspaces
+
+int pick_token_tile(int n, int E) {
+    // Test override: MOE_W4A16_TOKEN_TILE = 16, 32, 64 or 128.
+    static const int forced = [] {
+        const char *v = std::getenv("MOE_W4A16_TOKEN_TILE");
+        const int t = v ? std::atoi(v) : 0;
+        return (t == 16 || t == 32 || t == 64 || t == 128) ? t : 0;
+    }();
+    if (forced) return forced;
+    // rows per active expert if routing spreads the slots evenly
+    const int active = n < E ? (n > 0 ? n : 1) : E;
+    const int avg = (n + active - 1) / active;
+    int nt = 16;
+    while (nt < avg && nt < 128) nt <<= 1;
+    return nt;
+}
 
 AlignLayout align_layout(int, int, int) {
     AlignLayout l;
@@ -17,6 +37,9 @@ AlignLayout align_layout(int, int, int) {
 FwdLayout fwd_layout(int M, int k, int E, int H, int I) {
     const size_t n = (size_t)M * k;
     FwdLayout l;
+    l.nt = pick_token_tile((int)n, E);
+    l.max_tok_tiles = (int)(n / l.nt) + (n < (size_t)E ? (int)n : E) + 1;
+    l.grid = kMaxGrid;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t at = off;
@@ -29,6 +52,9 @@ FwdLayout fwd_layout(int M, int k, int E, int H, int I) {
     l.tile_prefix = take((size_t)(E + 1) * 4);
     l.perm = take(n * 4);
     l.inv_perm = take(n * 4);
+    // one ticket per (tile, epilogue warp)
+    l.tickets = take((size_t)l.max_tok_tiles * 4 * (2 * I / kTileRows + H / kTileRows) * 4);
+    l.partials = take((size_t)l.grid * 2 * l.nt * kTileRows * 4);
     l.xs = take(n * H * 2);
     l.act_hi = take(n * I * 2);
     l.act_lo = take(n * I * 2);
@@ -208,6 +234,14 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     moe_status_t st = check_device();
     if (st != MOE_OK) return st;
     if (M == 0) return MOE_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    int grid = tc_grid(dev);
+    if (grid <= 0) return MOE_ERR_CUDA;
+    if (grid > L.grid) grid = L.grid;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -217,46 +251,55 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     int32_t *tile_prefix = reinterpret_cast<int32_t *>(ws + L.tile_prefix);
     int32_t *perm = reinterpret_cast<int32_t *>(ws + L.perm);
     int32_t *inv_perm = reinterpret_cast<int32_t *>(ws + L.inv_perm);
+    int32_t *tickets = reinterpret_cast<int32_t *>(ws + L.tickets);
+    float *partials = reinterpret_cast<float *>(ws + L.partials);
     uint16_t *xs = reinterpret_cast<uint16_t *>(ws + L.xs);
     uint16_t *act_hi = reinterpret_cast<uint16_t *>(ws + L.act_hi);
     uint16_t *act_lo = reinterpret_cast<uint16_t *>(ws + L.act_lo);
     float *y = reinterpret_cast<float *>(ws + L.y);
     const int n = M * k;
-    const int tile = simple_token_tile();
+    const int r1 = 4 * (2 * I / kTileRows), r2 = 4 * (H / kTileRows);  // tickets per token tile
 
-    AlignArgs al = {ids, n, E, tile, counts, offsets, perm, inv_perm, tile_prefix, ctrl};
+    AlignArgs al = {ids, n, E, L.nt, counts, offsets, perm, inv_perm, tile_prefix, ctrl,
+                    tickets, r1, r2, L.max_tok_tiles * r1};
     GatherArgs ga = {hidden, perm, offsets, n, k, H, E, xs, ctrl};
-    GemmArgs g1 = {};
+    TcArgs g1 = {};
     g1.w_codes = static_cast<const uint8_t *>(w13);
     g1.w_scales = static_cast<const uint8_t *>(s13);
     g1.offsets = offsets;
-    g1.n = n;
+    g1.tile_prefix = tile_prefix;
+    g1.tickets = tickets;
+    g1.partials = partials;
     g1.E = E;
     g1.N = 2 * I;
     g1.K = H;
     g1.I = I;
     g1.kind = MOE_PACK_W13;
-    g1.in_hi = xs;
+    g1.nt = L.nt;
     g1.act_hi = act_hi;
     g1.act_lo = act_lo;
     g1.ctrl = ctrl;
-    GemmArgs g2 = g1;
+    TcArgs g2 = g1;
     g2.w_codes = static_cast<const uint8_t *>(w2);
     g2.w_scales = static_cast<const uint8_t *>(s2);
+    g2.tickets = tickets + L.max_tok_tiles * r1;
     g2.N = H;
     g2.K = I;
     g2.kind = MOE_PACK_W2;
-    g2.in_hi = act_hi;
-    g2.in_lo = act_lo;
     g2.y = y;
     CombineArgs cb = {y, inv_perm, topk_w, M, k, H, out};
+
+    CUtensorMap map_x, map_hi, map_lo;
+    if (!make_token_map(&map_x, xs, n, H, L.nt) || !make_token_map(&map_hi, act_hi, n, I, L.nt) ||
+        !make_token_map(&map_lo, act_lo, n, I, L.nt))
+        return MOE_ERR_CUDA;
 
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
     const bool pdl = (ev == nullptr);
     if (mark(0) != cudaSuccess || launch_align(al, s) != cudaSuccess || mark(1) != cudaSuccess ||
         launch_gather_hidden(ga, s, pdl) != cudaSuccess || mark(2) != cudaSuccess ||
-        launch_gemm_simple(g1, tile_prefix, s, pdl) != cudaSuccess || mark(3) != cudaSuccess ||
-        launch_gemm_simple(g2, tile_prefix, s, pdl) != cudaSuccess || mark(4) != cudaSuccess ||
+        launch_gemm_tc(g1, map_x, map_x, grid, s, pdl) != cudaSuccess || mark(3) != cudaSuccess ||
+        launch_gemm_tc(g2, map_hi, map_lo, grid, s, pdl) != cudaSuccess || mark(4) != cudaSuccess ||
         launch_combine(cb, s, pdl) != cudaSuccess || mark(5) != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;
@@ -266,9 +309,9 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     g_diag.E = E;
     g_diag.H = H;
     g_diag.I = I;
-    g_diag.token_tile = tile;
-    g_diag.grid_gemm1 = 0;
-    g_diag.grid_gemm2 = 0;
+    g_diag.token_tile = L.nt;
+    g_diag.grid_gemm1 = grid;
+    g_diag.grid_gemm2 = grid;
     g_diag.kernels_launched = 5;
     g_diag.workspace_bytes = (int64_t)L.total;
     g_diag.calls += 1;
@@ -309,6 +352,19 @@ moe_status_t moe_w4a16_get_device_status(const void *workspace, moe_stream_t str
     }
     if (detail) *detail = c.detail;
     return static_cast<moe_status_t>(c.status);
+}
+
+moe_status_t moe_w4a16_workspace_views(int M, int k, int E, int H, int I, moe_ws_views_t *v) {
+    if (!v || !layer_sizes_ok(M, k, E, H, I)) return MOE_ERR_INVALID_ARG;
+    const FwdLayout L = fwd_layout(M, k, E, H, I);
+    v->counts = L.counts;
+    v->offsets = L.offsets;
+    v->perm = L.perm;
+    v->inv_perm = L.inv_perm;
+    v->act_hi = L.act_hi;
+    v->act_lo = L.act_lo;
+    v->y = L.y;
+    return MOE_OK;
 }
 
 moe_status_t moe_w4a16_get_diag(moe_diag_t *diag) {

@@ -12,33 +12,30 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// One warp per sorted row; 16-byte loads and stores (8 elements per lane).
+// One thread per 16-byte chunk (8 elements) of a sorted row.
 __global__ void __launch_bounds__(kThreads) gather_hidden_kernel(GatherArgs a) {
     pdl_wait();
     pdl_trigger();
     const int valid = __ldg(a.offsets + a.E);
-    const int warps = kThreads / 32;
-    const int lane = threadIdx.x & 31;
     const int vecs = a.H / 8;
+    const int64_t total = (int64_t)valid * vecs;
     bool overflow = false;
-    for (int p = blockIdx.x * warps + (threadIdx.x >> 5); p < valid; p += gridDim.x * warps) {
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * kThreads) {
+        const int p = (int)(i / vecs), v = (int)(i % vecs);
         const int t = __ldg(a.perm + p) / a.k;
-        const uint4 *src = reinterpret_cast<const uint4 *>(a.hidden + (size_t)t * a.H);
-        uint4 *dst = reinterpret_cast<uint4 *>(a.xs + (size_t)p * a.H);
-        for (int v = lane; v < vecs; v += 32) {
-            const uint4 in = __ldg(src + v);
-            const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-            uint32_t o[4];
+        const uint4 in = __ldg(reinterpret_cast<const uint4 *>(a.hidden + (size_t)t * a.H) + v);
+        const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+        uint32_t o[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float lo = __uint_as_float(w[i] << 16);
-                const float hi = __uint_as_float(w[i] & 0xFFFF0000u);
-                overflow |= (fabsf(lo) > 65504.0f && !isinf(lo)) || (fabsf(hi) > 65504.0f && !isinf(hi));
-                const __half2 h = __floats2half2_rn(lo, hi);
-                o[i] = *reinterpret_cast<const uint32_t *>(&h);
-            }
-            dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(w[j] << 16);
+            const float hi = __uint_as_float(w[j] & 0xFFFF0000u);
+            overflow |= (fabsf(lo) > 65504.0f && !isinf(lo)) || (fabsf(hi) > 65504.0f && !isinf(hi));
+            const __half2 h = __floats2half2_rn(lo, hi);
+            o[j] = *reinterpret_cast<const uint32_t *>(&h);
         }
+        reinterpret_cast<uint4 *>(a.xs + (size_t)p * a.H)[v] = make_uint4(o[0], o[1], o[2], o[3]);
     }
     if (overflow) set_status(a.ctrl, MOE_ERR_DEVICE_FP16_RANGE, 0);
 }
@@ -89,8 +86,7 @@ cudaError_t launch(Kernel k, const Args &args, int blocks, cudaStream_t s, bool 
 }  // namespace
 
 cudaError_t launch_gather_hidden(const GatherArgs &a, cudaStream_t s, bool pdl) {
-    const int warps = kThreads / 32;
-    int64_t blocks = ((int64_t)a.n + warps - 1) / warps;
+    int64_t blocks = ((int64_t)a.n * (a.H / 8) + kThreads - 1) / kThreads;
     if (blocks > 152 * 16) blocks = 152 * 16;
     return launch(gather_hidden_kernel, a, (int)blocks, s, pdl);
 }

@@ -1,0 +1,570 @@
+// gemm_tc.cu -- grouped expert GEMMs on the 5th-generation tensor cores.
+//
+// Both expert contractions of the layer run here:
+//   gate+up (MOE_PACK_W13): for every expert-sorted token row p of expert e,
+//       g = xs[p] . Wg[n], u = xs[p] . Wu[n], a[p][n] = silu(g) * u  (the
+//       stacked gate+up GEMM of "perf(exl3): accelerate fat-expert prefill -
+//       #77", "Summary", with SiLU(gate)*up fused into the epilogue);
+//   down    (MOE_PACK_W2):  y[p][h] = (a_hi + a_lo)[p] . W2[h].
+// Weights are INT4 with one scale per 32 elements along K, as in the MoE
+// GEMM of "The MoE Throughput Lever: Quantifying the INT4 Marlin GEMM on
+// Blackwell PRO 6000" ("The Benchmark: What Was Measured").
+//
+// Design (weights as the MMA's M side, tokens as its N side):
+//  * One persistent CTA per SM.  The work is the list of tiles (expert,
+//    128-row weight tile, token tile of NT sorted rows) times 128-element K
+//    chunks; each CTA takes a contiguous, equal share of that list (stream-K),
+//    so the weight stream is spread evenly over all SMs even when only a few
+//    experts are active.  A tile cut between CTAs leaves fp32 partials in the
+//    workspace; the last CTA to finish it (an atomic ticket, no waiting)
+//    sums them in CTA order and runs the epilogue, so results do not depend
+//    on timing.
+//  * A TMA producer warp streams each chunk's 8 KiB code block and 1 KiB
+//    scale block (one bulk copy each) and the chunk's token rows (tensor
+//    copies, 128-byte swizzle) into a ring of shared-memory stages.
+//  * Two dequantisation warpgroups (alternating chunks) turn codes into
+//    exact fp16 weights, (q - 8) * scale, one weight row per thread, and
+//    write them straight into tensor memory with tcgen05.st.  That tensor
+//    memory is the A operand of tcgen05.mma, so dequantised weights never
+//    touch shared memory.
+//  * One thread issues tcgen05.mma (kind::f16, M = 128, N = token rows of the
+//    tile rounded up to 16, K = 16) accumulating in tensor memory; the down
+//    GEMM issues each step twice, for the hi and the lo halves of a.
+//  * An epilogue warpgroup drains the (double-buffered) accumulator while the
+//    next tile is being computed.
+// Every mbarrier wait is bounded; a wait that gives up records
+// MOE_ERR_DEVICE_TIMEOUT and the CTA winds down without hanging.
+#include <cstring>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "sm100.cuh"
+#include "gemm_tc.h"
+
+namespace moe {
+namespace {
+
+using namespace sm100;
+
+constexpr int kEpiWarps = 4;
+constexpr int kDqGroups = 2;
+constexpr int kThreads = 32 * (kEpiWarps + 4 * kDqGroups + 2);  // 448
+constexpr int kProducerWarp = kEpiWarps + 4 * kDqGroups;         // 12
+constexpr int kMmaWarp = kProducerWarp + 1;                      // 13
+constexpr int kABufs = 4;                     // TMEM A buffers (64 columns each)
+constexpr int kACols = kChunkK / 2;           // 64 fp16 pairs per row per chunk
+constexpr int kAccBase = kABufs * kACols;     // 256
+constexpr uint32_t kTmemCols = 512;
+constexpr long long kWaitCycles = 1ll << 31;  // bounded waits give up after ~1-2 s
+
+struct Smem {
+    uint64_t full[kMaxStages], empty[kMaxStages];
+    uint64_t a_full[kABufs], a_empty[kABufs];
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort;
+    int bad;
+};
+
+// Bounded wait that also gives up as soon as another role has aborted.  The
+// limit is measured with the SM's own cycle counter, which never runs
+// backwards.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Smem *sm, Ctrl *ctrl,
+                                         int who) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0) {
+            if (*(volatile int *)&sm->abort) return false;
+            if (clock64() - t0 > kWaitCycles) {
+                atomicExch(&sm->abort, 1);
+                set_status(ctrl, MOE_ERR_DEVICE_TIMEOUT, who);
+                return false;
+            }
+        }
+    }
+}
+
+// All lanes of a warp wait; the warp goes on only if every lane saw the
+// phase complete, so later warp-wide (.sync.aligned) instructions stay
+// convergent even when an abort races with completion.
+__device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, Smem *sm, Ctrl *ctrl,
+                                              int who) {
+    const bool ok = wait_bar(bar, parity, sm, ctrl, who);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait that ignores the abort flag (used while winding down).
+__device__ __forceinline__ bool wait_bar_final(uint64_t *bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+// Stream-K partition of W chunk-units over G CTAs.
+__device__ __forceinline__ int64_t range_begin(int g, int64_t W, int G) {
+    return (int64_t)g * W / G;
+}
+__device__ __forceinline__ int unit_owner(int64_t u, int64_t W, int G) {
+    return (int)(((u + 1) * (int64_t)G - 1) / W);
+}
+// Number of CTAs whose (non-empty) ranges cover units [u0, u1].
+__device__ __forceinline__ int contributors(int64_t u0, int64_t u1, int64_t W, int G) {
+    int n = 0;
+    for (int g = unit_owner(u0, W, G);; g = unit_owner(range_begin(g + 1, W, G), W, G)) {
+        ++n;
+        if (range_begin(g + 1, W, G) > u1) break;
+    }
+    return n;
+}
+
+struct Tile {
+    int e, rt, p0, rows;
+};
+
+template <int NT>
+__device__ __forceinline__ Tile decode_tile(const TcArgs &a, int tile) {
+    Tile t;
+    const int R = a.N / kTileRows;
+    t.e = find_segment(a.tile_prefix, a.E, tile / R);
+    const int tp0 = __ldg(a.tile_prefix + t.e), tp1 = __ldg(a.tile_prefix + t.e + 1);
+    const int local = tile - R * tp0, te = tp1 - tp0;
+    t.rt = local / te;
+    const int tt = local % te;
+    t.p0 = __ldg(a.offsets + t.e) + tt * NT;
+    t.rows = min(NT, __ldg(a.offsets + t.e + 1) - t.p0);
+    return t;
+}
+
+// (q - 8) * scale for the 8 codes of one word, as 4 fp16 pairs in element
+// order.  Nibbles are stored in element order 0,2,4,6,1,3,5,7, so masking
+// 0x000F000F yields elements (0,1), masking 0x00F000F0 yields 16x elements
+// (2,3), and the same after a shift by 8 gives (4,5) and (6,7).  OR-ing the
+// exponent of 1024 makes 1024 + q (or 1024 + 16q) exactly; subtracting 1032
+// (or scaling by 1/16 and adding -72) gives q - 8 exactly, and the product
+// with an fp16 scale of magnitude >= 2^-14 is exact (at most 11 bits).
+__device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, uint32_t (&o)[4]) {
+    const uint32_t magic = 0x64006400u;
+    const __half2 bias_lo = __floats2half2_rn(1032.f, 1032.f);
+    const __half2 sixteenth = __floats2half2_rn(0.0625f, 0.0625f);
+    const __half2 bias_hi = __floats2half2_rn(-72.f, -72.f);
+    const uint32_t w8 = w >> 8;
+    uint32_t r0 = (w & 0x000F000Fu) | magic;
+    uint32_t r1 = (w & 0x00F000F0u) | magic;
+    uint32_t r2 = (w8 & 0x000F000Fu) | magic;
+    uint32_t r3 = (w8 & 0x00F000F0u) | magic;
+    __half2 h0 = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&r0), bias_lo), s2);
+    __half2 h1 = __hmul2(__hfma2(*reinterpret_cast<__half2 *>(&r1), sixteenth, bias_hi), s2);
+    __half2 h2 = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&r2), bias_lo), s2);
+    __half2 h3 = __hmul2(__hfma2(*reinterpret_cast<__half2 *>(&r3), sixteenth, bias_hi), s2);
+    o[0] = *reinterpret_cast<uint32_t *>(&h0);
+    o[1] = *reinterpret_cast<uint32_t *>(&h1);
+    o[2] = *reinterpret_cast<uint32_t *>(&h2);
+    o[3] = *reinterpret_cast<uint32_t *>(&h3);
+}
+
+template <int KIND, int NT, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tok_hi,
+                   const __grid_constant__ CUtensorMap tok_lo) {
+    constexpr int kTokBox = NT * 128;                        // one 64-column box
+    constexpr int kTokBoxes = (KIND == MOE_PACK_W2) ? 4 : 2;  // hi(+lo) x 2 boxes
+    constexpr int kStageBytes = kTokBoxes * kTokBox + kCodeBlockBytes + kScaleBlockBytes;
+    static_assert(kStageBytes % 1024 == 0, "stage size must keep 1024-byte alignment");
+    static_assert(STAGES % kDqGroups == 0, "each stage must belong to one dequant group");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Smem *sm = reinterpret_cast<Smem *>(base + STAGES * kStageBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = gridDim.x, g = blockIdx.x;
+    const int R = a.N / kTileRows, KC = a.K / kChunkK;
+
+    // ---------------- setup
+    if (warp == kMmaWarp) {
+        tmem_alloc(&sm->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&sm->full[s], 1);
+            mbar_init(&sm->empty[s], 1);
+        }
+        for (int b = 0; b < kABufs; ++b) {
+            mbar_init(&sm->a_full[b], 128);
+            mbar_init(&sm->a_empty[b], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm->acc_full[b], 1);
+            mbar_init(&sm->acc_empty[b], 128);
+        }
+        mbar_init(&sm->done, 1);
+        sm->abort = 0;
+        sm->bad = !(header_ok(a.w_codes, KIND, kPartCodes, a.E, a.N, a.K) &&
+                    header_ok(a.w_scales, KIND, kPartScales, a.E, a.N, a.K));
+        if (sm->bad && g == 0) set_status(a.ctrl, MOE_ERR_BAD_LAYOUT, KIND);
+        fence_barrier_init();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tensormap(&tok_hi);
+        if (KIND == MOE_PACK_W2) prefetch_tensormap(&tok_lo);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_trigger();
+
+    const uint32_t tb = sm->tmem_base;
+    const int64_t W = sm->bad ? 0 : (int64_t)__ldg(a.tile_prefix + a.E) * R * KC;
+    const int64_t u_begin = range_begin(g, W, G), u_end = range_begin(g + 1, W, G);
+    const int my_chunks = (int)(u_end - u_begin);
+
+    if (warp == kProducerWarp) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            pdl_wait();  // token rows come from the previous kernel
+            int c = 0;
+            bool ok = true;
+            for (int64_t u = u_begin; u < u_end && ok;) {
+                const int tile = (int)(u / KC), k0 = (int)(u % KC);
+                const int k1 = (int)min((int64_t)KC, k0 + (u_end - u));
+                const Tile t = decode_tile<NT>(a, tile);
+                for (int kc = k0; kc < k1; ++kc, ++c) {
+                    const int s = c % STAGES;
+                    if (!wait_bar(&sm->empty[s], ((c / STAGES) & 1) ^ 1, sm, a.ctrl, 1)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *st = base + s * kStageBytes;
+                    mbar_arrive_expect_tx(&sm->full[s], kStageBytes);
+                    const int64_t blk = ((int64_t)t.e * R + t.rt) * KC + kc;
+                    bulk_g2s(st + kTokBoxes * kTokBox,
+                             a.w_codes + kHeaderBytes + blk * kCodeBlockBytes, kCodeBlockBytes,
+                             &sm->full[s]);
+                    bulk_g2s(st + kTokBoxes * kTokBox + kCodeBlockBytes,
+                             a.w_scales + kHeaderBytes + blk * kScaleBlockBytes, kScaleBlockBytes,
+                             &sm->full[s]);
+                    const int x0 = kc * kChunkK;
+                    tma_load_2d(st, &tok_hi, x0, t.p0, &sm->full[s]);
+                    tma_load_2d(st + kTokBox, &tok_hi, x0 + 64, t.p0, &sm->full[s]);
+                    if (KIND == MOE_PACK_W2) {
+                        tma_load_2d(st + 2 * kTokBox, &tok_lo, x0, t.p0, &sm->full[s]);
+                        tma_load_2d(st + 3 * kTokBox, &tok_lo, x0 + 64, t.p0, &sm->full[s]);
+                    }
+                }
+                u += k1 - k0;
+            }
+            // Before the CTA exits, every copy this thread issued must have
+            // landed; after an abort elsewhere some were never consumed.  The
+            // last copy into each stage is the only one that can be pending.
+            const int issued = c;
+            for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j)
+                wait_bar_final(&sm->full[j % STAGES], (j / STAGES) & 1);
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            int c = 0, seg = 0;
+            bool ok = true;
+            for (int64_t u = u_begin; u < u_end && ok; ++seg) {
+                const int tile = (int)(u / KC), k0 = (int)(u % KC);
+                const int k1 = (int)min((int64_t)KC, k0 + (u_end - u));
+                const Tile t = decode_tile<NT>(a, tile);
+                const int n_mma = max(16, (t.rows + 15) & ~15);
+                const uint32_t idesc = idesc_f16_m128((uint32_t)n_mma);
+                const int acc = seg & 1;
+                if (!wait_bar(&sm->acc_empty[acc], ((seg >> 1) & 1) ^ 1, sm, a.ctrl, 2)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tb + kAccBase + acc * NT;
+                for (int kc = k0; kc < k1; ++kc, ++c) {
+                    const int s = c % STAGES, b = c % kABufs;
+                    if (!wait_bar(&sm->a_full[b], (c / kABufs) & 1, sm, a.ctrl, 3)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = smem_u32(base + s * kStageBytes);
+                    const uint32_t a_tmem = tb + b * kACols;
+#pragma unroll
+                    for (int j = 0; j < kChunkK / 16; ++j) {
+                        const uint32_t boff = (j >> 2) * kTokBox + (j & 3) * 32;
+                        mma_f16_ts(d_tmem, a_tmem + j * 8, sdesc_k_sw128(st + boff), idesc,
+                                   (kc > k0 || j > 0) ? 1u : 0u);
+                        if (KIND == MOE_PACK_W2)
+                            mma_f16_ts(d_tmem, a_tmem + j * 8,
+                                       sdesc_k_sw128(st + 2 * kTokBox + boff), idesc, 1u);
+                    }
+                    tc_commit(&sm->empty[s]);
+                    tc_commit(&sm->a_empty[b]);
+                }
+                if (!ok) break;
+                tc_commit(&sm->acc_full[acc]);
+                u += k1 - k0;
+            }
+            // Every MMA this thread issued has completed once `done` fires.
+            tc_commit(&sm->done);
+            wait_bar_final(&sm->done, 0);
+        }
+    } else if (warp >= kEpiWarps) {
+        // ---------------- dequantisation warpgroups
+        const int grp = (warp - kEpiWarps) / 4;
+        const int r = (warp & 3) * 32 + lane;  // weight row of the tile = TMEM lane
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        for (int c = grp; c < my_chunks; c += kDqGroups) {
+            const int s = c % STAGES, b = c % kABufs;
+            if (!warp_wait_bar(&sm->full[s], (c / STAGES) & 1, sm, a.ctrl, 4)) break;
+            if (!warp_wait_bar(&sm->a_empty[b], ((c / kABufs) & 1) ^ 1, sm, a.ctrl, 5)) break;
+            tc_fence_after();
+            const uint8_t *st = base + s * kStageBytes + kTokBoxes * kTokBox;
+            const uint2 sc = *reinterpret_cast<const uint2 *>(st + kCodeBlockBytes + r * 8);
+            const uint32_t scw[2] = {sc.x, sc.y};
+            const uint32_t a_addr = tb + lane_off + b * kACols;
+#pragma unroll
+            for (int pc = 0; pc < 4; ++pc) {
+                const uint4 q = *reinterpret_cast<const uint4 *>(st + (pc * kTileRows + r) * 16);
+                const uint32_t sbits = (scw[pc >> 1] >> ((pc & 1) * 16)) & 0xFFFFu;
+                const __half hs = __ushort_as_half((unsigned short)sbits);
+                const __half2 s2 = __halves2half2(hs, hs);
+                uint32_t v[16];
+                uint32_t o[4];
+                dequant_word(q.x, s2, o);
+                v[0] = o[0]; v[1] = o[1]; v[2] = o[2]; v[3] = o[3];
+                dequant_word(q.y, s2, o);
+                v[4] = o[0]; v[5] = o[1]; v[6] = o[2]; v[7] = o[3];
+                dequant_word(q.z, s2, o);
+                v[8] = o[0]; v[9] = o[1]; v[10] = o[2]; v[11] = o[3];
+                dequant_word(q.w, s2, o);
+                v[12] = o[0]; v[13] = o[1]; v[14] = o[2]; v[15] = o[3];
+                tmem_st16(a_addr + pc * 16, v);
+            }
+            tc_wait_st();
+            tc_fence_before();
+            mbar_arrive(&sm->a_full[b]);
+        }
+    } else {
+        // ---------------- epilogue warpgroup (warps 0-3)
+        const int r = warp * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        float *part = a.partials;
+        int seg = 0;
+        for (int64_t u = u_begin; u < u_end; ++seg) {
+            const int tile = (int)(u / KC), k0 = (int)(u % KC);
+            const int k1 = (int)min((int64_t)KC, k0 + (u_end - u));
+            const Tile t = decode_tile<NT>(a, tile);
+            const int acc = seg & 1;
+            if (!warp_wait_bar(&sm->acc_full[acc], (seg >> 1) & 1, sm, a.ctrl, 6)) break;
+            tc_fence_after();
+            const uint32_t acc_addr = tb + lane_off + kAccBase + acc * NT;
+            const bool whole = (k0 == 0 && k1 == KC);
+            const int which = (u == u_begin) ? 0 : 1;  // first or last segment of this CTA
+            float *slot = part + ((size_t)g * 2 + which) * (size_t)NT * kTileRows;
+#pragma unroll 1
+            for (int c0 = 0; c0 < t.rows; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(acc_addr + c0, v);
+                tc_wait_ld();
+                if (whole) {
+                    {
+                        if (KIND == MOE_PACK_W13) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const float mine = __uint_as_float(v[j]);
+                                const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+                                if (c0 + j < t.rows) {
+                                    const float gte = (lane & 1) ? other : mine;
+                                    const float up = (lane & 1) ? mine : other;
+                                    const float act = gte / (1.0f + expf(-gte)) * up;
+                                    const __half hi = __float2half_rn(act);
+                                    const size_t o = (size_t)(t.p0 + c0 + j) * a.I +
+                                                     t.rt * (kTileRows / 2) + (r >> 1);
+                                    if (lane & 1) {
+                                        const __half lo = __float2half_rn(act - __half2float(hi));
+                                        a.act_lo[o] = __half_as_ushort(lo);
+                                    } else {
+                                        a.act_hi[o] = __half_as_ushort(hi);
+                                        if (fabsf(act) > 65504.0f && !isinf(act) && !isnan(act))
+                                            set_status(a.ctrl, MOE_ERR_DEVICE_FP16_RANGE, 1);
+                                    }
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                if (c0 + j < t.rows)
+                                    a.y[(size_t)(t.p0 + c0 + j) * a.N + t.rt * kTileRows + r] =
+                                        __uint_as_float(v[j]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        slot[(size_t)(c0 + j) * kTileRows + r] = __uint_as_float(v[j]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&sm->acc_empty[acc]);
+
+            if (!whole) {
+                // Fixed-order reduction by whichever CTA finishes the tile
+                // last; each warp handles its own 32 rows with its own ticket.
+                const int64_t tu0 = (int64_t)tile * KC, tu1 = tu0 + KC - 1;
+                const int ncontrib = contributors(tu0, tu1, W, G);
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) last = (atomicAdd(a.tickets + (size_t)tile * 4 + warp, 1) == ncontrib - 1);
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+#pragma unroll 1
+                    for (int col = 0; col < t.rows; ++col) {
+                        float sum = 0.f;
+                        for (int gg = unit_owner(tu0, W, G);; gg = unit_owner(range_begin(gg + 1, W, G), W, G)) {
+                            const int wh = (range_begin(gg, W, G) >= tu0) ? 0 : 1;
+                            const float *sl = part + ((size_t)gg * 2 + wh) * (size_t)NT * kTileRows;
+                            sum += __ldcg(sl + (size_t)col * kTileRows + r);
+                            if (range_begin(gg + 1, W, G) > tu1) break;
+                        }
+                        if (KIND == MOE_PACK_W13) {
+                            const float other = __shfl_xor_sync(0xffffffffu, sum, 1);
+                            const float gte = (lane & 1) ? other : sum;
+                            const float up = (lane & 1) ? sum : other;
+                            const float act = gte / (1.0f + expf(-gte)) * up;
+                            const __half hi = __float2half_rn(act);
+                            const size_t o = (size_t)(t.p0 + col) * a.I + t.rt * (kTileRows / 2) +
+                                             (r >> 1);
+                            if (lane & 1) {
+                                a.act_lo[o] = __half_as_ushort(__float2half_rn(act - __half2float(hi)));
+                            } else {
+                                a.act_hi[o] = __half_as_ushort(hi);
+                                if (fabsf(act) > 65504.0f && !isinf(act) && !isnan(act))
+                                    set_status(a.ctrl, MOE_ERR_DEVICE_FP16_RANGE, 1);
+                            }
+                        } else {
+                            a.y[(size_t)(t.p0 + col) * a.N + t.rt * kTileRows + r] = sum;
+                        }
+                    }
+                }
+            }
+            u += k1 - k0;
+        }
+    }
+
+    // ---------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tb, kTmemCols);
+    }
+}
+
+using KernelFn = void (*)(const TcArgs, const CUtensorMap, const CUtensorMap);
+
+template <int KIND, int NT>
+struct Config {
+    static constexpr int kTokBoxes = (KIND == MOE_PACK_W2) ? 4 : 2;
+    static constexpr int kStage = kTokBoxes * NT * 128 + kCodeBlockBytes + kScaleBlockBytes;
+    static constexpr int kBudget = 210 * 1024;
+    // An even stage count keeps every shared-memory stage with one dequant
+    // warpgroup (chunk c and chunk c + kStages have the same parity), so a
+    // warpgroup always waits on the phase right after the one it consumed
+    // and the parity test of the mbarrier cannot alias an older phase.
+    static constexpr int kFit = (kBudget / kStage) < kMaxStages ? (kBudget / kStage) : kMaxStages;
+    static constexpr int kStages = kFit & ~1;
+    static_assert(kStages >= 2 && kStages % kDqGroups == 0, "stage count must be a multiple of the dequant groups");
+    static constexpr size_t kSmem = (size_t)kStages * kStage + sizeof(Smem) + 1024;
+    static KernelFn fn() { return gemm_tc_kernel<KIND, NT, kStages>; }
+};
+
+template <int KIND>
+bool pick(int nt, KernelFn *fn, size_t *smem) {
+    switch (nt) {
+        case 16: *fn = Config<KIND, 16>::fn(); *smem = Config<KIND, 16>::kSmem; return true;
+        case 32: *fn = Config<KIND, 32>::fn(); *smem = Config<KIND, 32>::kSmem; return true;
+        case 64: *fn = Config<KIND, 64>::fn(); *smem = Config<KIND, 64>::kSmem; return true;
+        case 128: *fn = Config<KIND, 128>::fn(); *smem = Config<KIND, 128>::kSmem; return true;
+    }
+    return false;
+}
+
+// ---------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+}  // namespace
+
+bool make_token_map(CUtensorMap *map, const void *ptr, int rows, int cols, int box_rows) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+int tc_grid(int device) {
+    static int sms[64] = {0};
+    if (device < 0 || device >= 64) return 0;
+    if (!sms[device]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        sms[device] = v;
+    }
+    return sms[device];
+}
+
+cudaError_t launch_gemm_tc(const TcArgs &args, const CUtensorMap &hi, const CUtensorMap &lo,
+                           int grid, cudaStream_t s, bool pdl) {
+    KernelFn fn = nullptr;
+    size_t smem = 0;
+    const bool ok = (args.kind == MOE_PACK_W13) ? pick<MOE_PACK_W13>(args.nt, &fn, &smem)
+                                                : pick<MOE_PACK_W2>(args.nt, &fn, &smem);
+    if (!ok) return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, fn, args, hi, lo);
+}
+
+}  // namespace moe

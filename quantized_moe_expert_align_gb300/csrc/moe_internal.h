@@ -76,13 +76,20 @@ AlignLayout align_layout(int M, int k, int E);
 
 // Carving of the forward workspace.
 struct FwdLayout {
+    int nt;             // token rows per MMA tile
+    int max_tok_tiles;  // bound on sum_e ceil(count_e / nt)
+    int grid;           // most CTAs the GEMM kernels may use (partials are sized for it)
     size_t ctrl, counts, offsets, tile_prefix, perm, inv_perm;
+    size_t tickets;     // int32 [max_tok_tiles * (2I/128 + H/128)]
+    size_t partials;    // fp32 [grid][2][nt][128]
     size_t xs;          // [n][H] fp16 hidden rows in sorted order
     size_t act_hi;      // [n][I] fp16
     size_t act_lo;      // [n][I] fp16
     size_t y;           // [n][H] fp32
     size_t total;
 };
+// Token rows per tile for a batch of n = M*k slots over E experts.
+int pick_token_tile(int n, int E);
 FwdLayout fwd_layout(int M, int k, int E, int H, int I);
 
 // ---------------------------------------------------------------------------
@@ -95,6 +102,8 @@ struct AlignArgs {
     int token_tile;   // >0: also write tile_prefix for this tile width
     int32_t *counts, *offsets, *perm, *inv_perm, *tile_prefix;
     Ctrl *ctrl;
+    int32_t *tickets; // if non-null: zero tiles*r1 entries at 0 and tiles*r2 at off2
+    int r1, r2, off2;
 };
 cudaError_t launch_align(const AlignArgs &a, cudaStream_t s);
 
@@ -113,21 +122,6 @@ struct GatherArgs {
 };
 cudaError_t launch_gather_hidden(const GatherArgs &a, cudaStream_t s, bool pdl);
 
-struct GemmArgs {
-    const uint8_t *w_codes;   // prepacked buffer (header included)
-    const uint8_t *w_scales;
-    const int32_t *offsets;   // [E+1]
-    int n, E, N, K, I;        // N, K of this matrix; I for the w13 epilogue
-    int kind;                 // MOE_PACK_W13 or MOE_PACK_W2
-    const uint16_t *in_hi;    // [n][K] fp16 operand rows (sorted order)
-    const uint16_t *in_lo;    // [n][K] fp16 low parts (w2 only) or null
-    uint16_t *act_hi, *act_lo;  // w13 output [n][I]
-    float *y;                 // w2 output [n][N]
-    Ctrl *ctrl;
-};
-cudaError_t launch_gemm_simple(const GemmArgs &a, const int32_t *tile_prefix, cudaStream_t s,
-                               bool pdl);
-int simple_token_tile();
 
 struct CombineArgs {
     const float *y;           // [n][H]

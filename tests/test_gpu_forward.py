@@ -62,3 +62,54 @@ def test_duplicate_ids_and_ragged(toy_layer):
     w = rng.random((M, L.k)).astype(np.float32)
     out, _ = toy_layer.forward(x, ids, w)
     gu.parity(gu.bf16_dev_to_f64(out), toy_layer.oracle(x, ids, w), "toy duplicates")
+
+
+# ---- larger batches: the forward runs on the whole batch, the oracle on a sample
+@pytest.mark.parametrize("M", [256, 512, 1024])
+def test_plateau_e384_sampled(e384_layer, M):
+    _check(e384_layer, synth.PLATEAU, M, sample=24)
+
+
+@pytest.mark.parametrize("M", [4096, 16384])
+def test_prefill_zipf_e384_sampled(e384_layer, M):
+    _check(e384_layer, synth.PREFILL, M, sample=16)
+
+
+@pytest.mark.parametrize("M", [256, 2048])
+def test_second_shape_sampled(e128_layer, M):
+    _check(e128_layer, synth.SECOND, M, sample=24)
+
+
+def test_token_tile_64(e128_layer):
+    """A batch whose rows per expert select 64-row token tiles."""
+    import quantized_moe_expert_align_gb300 as moe
+    _check(e128_layer, synth.SECOND, 800, sample=24)
+    assert moe.moe_w4a16_get_diag()["token_tile"] == 64
+
+
+# ---- stage-level checks: the sorted intermediates against the oracle's
+def _stages(dl, wl, M, rows_cap=None):
+    import quantized_moe_expert_align_gb300 as moe
+    L = wl.layer
+    x, ids, w = _inputs(wl, M)
+    out, ws = dl.forward(x, ids, w)
+    inter = moe.intermediates(ws, M, L.k, L.E, L.H, L.I)
+    import oracle
+    ref = oracle.forward(x, ids, w, dl.w13, dl.s13, dl.w2, dl.s2, L.E, L.H, L.I,
+                         want_intermediates=True)
+    assert np.array_equal(inter["offsets"], ref["offsets"])
+    n = int(ref["offsets"][-1])
+    assert np.array_equal(inter["perm"][:n], ref["perm"][:n])
+    for name, got, exp in [("act", inter["act"], ref["act"]), ("y", inter["y"], ref["y"])]:
+        d = np.abs(got - exp)
+        tol = 1e-3 + 1e-3 * np.abs(exp)
+        assert np.all(d <= tol), f"{name}: {int(np.sum(d > tol))} bad, max d/tol {float(np.max(d / tol)):.3f}"
+
+
+def test_stages_toy(toy_layer):
+    _stages(toy_layer, synth.TOY, 4)
+
+
+@pytest.mark.parametrize("M", [1, 9])
+def test_stages_decode(e384_layer, M):
+    _stages(e384_layer, synth.DECODE, M)
