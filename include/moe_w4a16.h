@@ -179,6 +179,45 @@ moe_status_t moe_w4a16_forward_profiled(const uint16_t *hidden, const int32_t *t
                                         moe_stream_t stream, void **events, int n_events);
 
 /*
+ * Size of the device array that moe_w4a16_forward_static uses as its
+ * workspace: 16 MiB, reserved on every GPU that loads this library.
+ */
+#define MOE_W4A16_STATIC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * moe_w4a16_forward without a caller-provided workspace, for callers that
+ * cannot allocate device memory: code embedded in a host framework that owns
+ * every device allocation and hands out only its own tensors, or a
+ * latency-bound decode loop where cudaMalloc would synchronise the device.
+ * (The pages describe no such entry point; it is a convenience of this
+ * library.)
+ *
+ *  Arguments, layouts and results are those of moe_w4a16_forward; hidden,
+ *  ids, weights and out are still the caller's.  Instead of a workspace the
+ *  call uses one device array of MOE_W4A16_STATIC_SCRATCH_BYTES inside the
+ *  library.  It allocates nothing: no cudaMalloc, cudaFree or other
+ *  allocating routine.
+ *  - Sizes whose moe_w4a16_workspace_size exceeds the array are rejected
+ *    with MOE_ERR_WORKSPACE_TOO_SMALL before anything is launched (at E=384,
+ *    H=7168, I=2048, top-8 that admits M up to about 24 tokens).
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before
+ *    any stream capture.
+ *  - Every call on a device shares the one array and it keeps the last
+ *    call's contents; the call itself resets what must start at zero (the
+ *    status word and the split-K tickets).  Calls that overlap on the GPU
+ *    (different streams, or the same array used from two threads without
+ *    ordering) race and give undefined results.
+ *  - Device-detected errors are recorded in the array's status word, which
+ *    moe_w4a16_get_device_status cannot reach: use moe_w4a16_forward with a
+ *    workspace when those errors must be observed.
+ */
+moe_status_t moe_w4a16_forward_static(const uint16_t *hidden, const int32_t *topk_ids,
+                                      const float *topk_w, const void *w13, const void *s13,
+                                      const void *w2, const void *s2, uint16_t *out, int M,
+                                      int k, int E, int H, int I, moe_stream_t stream);
+
+/*
  * Wait for `stream`, then return the status word the device recorded in
  * `workspace` during the most recent align/forward call on it (MOE_OK if
  * nothing went wrong).  `detail` (may be NULL) receives a code-specific

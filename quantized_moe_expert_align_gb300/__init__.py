@@ -75,6 +75,7 @@ def load(path: str = LIB_PATH):
             "moe_w4a16_forward": (i, [p, p, p, p, p, p, p, p, i, i, i, i, i, p, sz, p]),
             "moe_w4a16_forward_profiled": (i, [p, p, p, p, p, p, p, p, i, i, i, i, i, p, sz, p,
                                                ctypes.POINTER(p), i]),
+            "moe_w4a16_forward_static": (i, [p, p, p, p, p, p, p, p, i, i, i, i, i, p]),
             "moe_w4a16_get_device_status": (i, [p, p, ctypes.POINTER(ctypes.c_int32)]),
             "moe_w4a16_get_diag": (i, [ctypes.POINTER(moe_diag_t)]),
             "moe_w4a16_workspace_views": (i, [i, i, i, i, i, ctypes.POINTER(moe_ws_views_t)]),
@@ -151,6 +152,16 @@ def moe_w4a16_forward_profiled(hidden, topk_ids, topk_w, w13, s13, w2, s2, out, 
         _p(hidden), _p(topk_ids), _p(topk_w), _p(w13), _p(s13), _p(w2), _p(s2), _p(out), M, k, E,
         H, I, _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream), arr,
         len(events))
+
+
+def moe_w4a16_forward_static(hidden, topk_ids, topk_w, w13, s13, w2, s2, out, M, k, E, H, I,
+                             stream=None):
+    """The forward on the library's static device scratch (no workspace)."""
+    return load().moe_w4a16_forward_static(_p(hidden), _p(topk_ids), _p(topk_w), _p(w13), _p(s13),
+                                           _p(w2), _p(s2), _p(out), M, k, E, H, I, _stream(stream))
+
+
+MOE_W4A16_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 def moe_w4a16_get_device_status(workspace, stream=None):

@@ -374,3 +374,17 @@ moe_status_t moe_w4a16_get_diag(moe_diag_t *diag) {
 }
 
 }  // extern "C"
+
+namespace moe {
+
+// The forward on a caller-chosen scratch buffer (used by the entry point
+// whose scratch is a static device array).
+moe_status_t forward_on_scratch(const uint16_t *hidden, const int32_t *ids, const float *topk_w,
+                                const void *w13, const void *s13, const void *w2, const void *s2,
+                                uint16_t *out, int M, int k, int E, int H, int I, void *scratch,
+                                size_t scratch_bytes, moe_stream_t stream) {
+    return forward_impl(hidden, ids, topk_w, w13, s13, w2, s2, out, M, k, E, H, I, scratch,
+                        scratch_bytes, stream, nullptr);
+}
+
+}  // namespace moe

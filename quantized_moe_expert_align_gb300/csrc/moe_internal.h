@@ -92,6 +92,12 @@ struct FwdLayout {
 int pick_token_tile(int n, int E);
 FwdLayout fwd_layout(int M, int k, int E, int H, int I);
 
+// moe_w4a16_forward on a scratch buffer the caller of this function chose.
+moe_status_t forward_on_scratch(const uint16_t *hidden, const int32_t *ids, const float *topk_w,
+                                const void *w13, const void *s13, const void *w2, const void *s2,
+                                uint16_t *out, int M, int k, int E, int H, int I, void *scratch,
+                                size_t scratch_bytes, moe_stream_t stream);
+
 // ---------------------------------------------------------------------------
 // Launchers (each returns the cudaError_t of its launch).
 // ---------------------------------------------------------------------------
