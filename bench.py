@@ -252,8 +252,10 @@ def our_arm(args, wl):
     torch.cuda.synchronize()
 
     # ---- timed region: K steps, device time per step, L2 flushed between ----
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # Events also mark each call inside a step (the first kernel of a call
+    # waits for the previous call anyway, so they do not change the timing).
+    nM = len(wl.Ms)
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nM + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -262,14 +264,17 @@ def our_arm(args, wl):
     torch.cuda.synchronize()
     for i in range(args.steps):
         flush.zero_()
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
+        marks[i][0].record(stream)
+        for j, M in enumerate(wl.Ms):
+            call(M)
+            marks[i][j + 1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    step_ms = [m[0].elapsed_time(m[nM]) for m in marks]
+    call_ms = {M: float(np.mean([m[j].elapsed_time(m[j + 1]) for m in marks]))
+               for j, M in enumerate(wl.Ms)}
     total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
@@ -310,6 +315,8 @@ def our_arm(args, wl):
         t_roof_ms = 1e3 * max(roof_bytes / (hbm_peak * 1e9), flops / (tf_peak * 1e12))
         sweep.append({
             "M": M, "active_experts": active,
+            "us_per_call": round(1e3 * call_ms[M], 2), "tokens_per_s": round(M / (call_ms[M] / 1e3), 1),
+            "frac_of_roofline": round(t_roof_ms / call_ms[M], 4),
             "kernel_ms": {n: round(float(v), 5) for n, v in zip(KERNELS, k_ms)},
             "us_per_call_profiled": round(1e3 * float(k_ms.sum()), 2),
             "roofline_bytes": roof_bytes, "roofline_us": round(1e3 * t_roof_ms, 2),

@@ -51,15 +51,15 @@ constexpr int kDqGroups = 2;
 constexpr int kThreads = 32 * (kEpiWarps + 4 * kDqGroups + 2);  // 448
 constexpr int kProducerWarp = kEpiWarps + 4 * kDqGroups;         // 12
 constexpr int kMmaWarp = kProducerWarp + 1;                      // 13
-constexpr int kABufs = 4;                     // TMEM A buffers (64 columns each)
+constexpr int kMaxABufs = 4;                  // TMEM A buffers (64 columns each)
 constexpr int kACols = kChunkK / 2;           // 64 fp16 pairs per row per chunk
-constexpr int kAccBase = kABufs * kACols;     // 256
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitCycles = 1ll << 31;  // bounded waits give up after ~1-2 s
 
 struct Smem {
-    uint64_t full[kMaxStages], empty[kMaxStages];
-    uint64_t a_full[kABufs], a_empty[kABufs];
+    uint64_t full[kMaxStages];      // stage loaded (TMA transaction bytes)
+    uint64_t consumed[kMaxStages];  // MMAs of the stage's chunk done (stage and A buffer free)
+    uint64_t a_full[kMaxABufs];     // A buffer written by the dequant warps
     uint64_t acc_full[2], acc_empty[2];
     uint64_t done;
     uint32_t tmem_base;
@@ -173,6 +173,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kTokBox = NT * 128;                        // one 64-column box
     constexpr int kTokBoxes = (KIND == MOE_PACK_W2) ? 4 : 2;  // hi(+lo) x 2 boxes
     constexpr int kStageBytes = kTokBoxes * kTokBox + kCodeBlockBytes + kScaleBlockBytes;
+    // Down GEMM with small token tiles: the hi and lo rows of a are stacked
+    // into one B operand of 2*NT rows, so one MMA (whose cost does not grow
+    // with N up to 128) covers both; the epilogue adds the two halves.
+    constexpr bool kCat = (KIND == MOE_PACK_W2) && (NT <= 64);
+    constexpr int kAB = (STAGES >= 4) ? 4 : 2;               // TMEM A buffers in use
+    constexpr int kAccBase = kAB * kACols;
+    constexpr int kAccCols = kCat ? 2 * NT : NT;              // columns per accumulator
+    static_assert(kAccBase + 2 * kAccCols <= 512, "tensor memory budget");
+    static_assert(STAGES >= kAB, "a stage must outlive its A buffer's reuse distance");
     static_assert(kStageBytes % 1024 == 0, "stage size must keep 1024-byte alignment");
     static_assert(STAGES % kDqGroups == 0, "each stage must belong to one dequant group");
 
@@ -193,12 +202,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&sm->full[s], 1);
-            mbar_init(&sm->empty[s], 1);
+            mbar_init(&sm->consumed[s], 1);
         }
-        for (int b = 0; b < kABufs; ++b) {
-            mbar_init(&sm->a_full[b], 128);
-            mbar_init(&sm->a_empty[b], 1);
-        }
+        for (int b = 0; b < kAB; ++b) mbar_init(&sm->a_full[b], 128);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm->acc_full[b], 1);
             mbar_init(&sm->acc_empty[b], 128);
@@ -236,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Tile t = decode_tile<NT>(a, tile);
                 for (int kc = k0; kc < k1; ++kc, ++c) {
                     const int s = c % STAGES;
-                    if (!wait_bar(&sm->empty[s], ((c / STAGES) & 1) ^ 1, sm, a.ctrl, 1)) {
+                    if (!wait_bar(&sm->consumed[s], ((c / STAGES) & 1) ^ 1, sm, a.ctrl, 1)) {
                         ok = false;
                         break;
                     }
@@ -250,9 +256,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                              a.w_scales + kHeaderBytes + blk * kScaleBlockBytes, kScaleBlockBytes,
                              &sm->full[s]);
                     const int x0 = kc * kChunkK;
-                    tma_load_2d(st, &tok_hi, x0, t.p0, &sm->full[s]);
-                    tma_load_2d(st + kTokBox, &tok_hi, x0 + 64, t.p0, &sm->full[s]);
-                    if (KIND == MOE_PACK_W2) {
+                    if (KIND == MOE_PACK_W13) {
+                        tma_load_2d(st, &tok_hi, x0, t.p0, &sm->full[s]);
+                        tma_load_2d(st + kTokBox, &tok_hi, x0 + 64, t.p0, &sm->full[s]);
+                    } else if (kCat) {  // [hi | lo] for K 0-63, then for K 64-127
+                        tma_load_2d(st, &tok_hi, x0, t.p0, &sm->full[s]);
+                        tma_load_2d(st + kTokBox, &tok_lo, x0, t.p0, &sm->full[s]);
+                        tma_load_2d(st + 2 * kTokBox, &tok_hi, x0 + 64, t.p0, &sm->full[s]);
+                        tma_load_2d(st + 3 * kTokBox, &tok_lo, x0 + 64, t.p0, &sm->full[s]);
+                    } else {            // [hi K0-63 | hi K64-127 | lo K0-63 | lo K64-127]
+                        tma_load_2d(st, &tok_hi, x0, t.p0, &sm->full[s]);
+                        tma_load_2d(st + kTokBox, &tok_hi, x0 + 64, t.p0, &sm->full[s]);
                         tma_load_2d(st + 2 * kTokBox, &tok_lo, x0, t.p0, &sm->full[s]);
                         tma_load_2d(st + 3 * kTokBox, &tok_lo, x0 + 64, t.p0, &sm->full[s]);
                     }
@@ -275,15 +289,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int tile = (int)(u / KC), k0 = (int)(u % KC);
                 const int k1 = (int)min((int64_t)KC, k0 + (u_end - u));
                 const Tile t = decode_tile<NT>(a, tile);
-                const int n_mma = max(16, (t.rows + 15) & ~15);
+                const int n_mma = kCat ? 2 * NT : max(16, (t.rows + 15) & ~15);
                 const uint32_t idesc = idesc_f16_m128((uint32_t)n_mma);
                 const int acc = seg & 1;
                 if (!wait_bar(&sm->acc_empty[acc], ((seg >> 1) & 1) ^ 1, sm, a.ctrl, 2)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tb + kAccBase + acc * NT;
+                const uint32_t d_tmem = tb + kAccBase + acc * kAccCols;
                 for (int kc = k0; kc < k1; ++kc, ++c) {
-                    const int s = c % STAGES, b = c % kABufs;
-                    if (!wait_bar(&sm->a_full[b], (c / kABufs) & 1, sm, a.ctrl, 3)) {
+                    const int s = c % STAGES, b = c % kAB;
+                    if (!wait_bar(&sm->a_full[b], (c / kAB) & 1, sm, a.ctrl, 3)) {
                         ok = false;
                         break;
                     }
@@ -292,15 +306,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a_tmem = tb + b * kACols;
 #pragma unroll
                     for (int j = 0; j < kChunkK / 16; ++j) {
-                        const uint32_t boff = (j >> 2) * kTokBox + (j & 3) * 32;
-                        mma_f16_ts(d_tmem, a_tmem + j * 8, sdesc_k_sw128(st + boff), idesc,
-                                   (kc > k0 || j > 0) ? 1u : 0u);
-                        if (KIND == MOE_PACK_W2)
-                            mma_f16_ts(d_tmem, a_tmem + j * 8,
-                                       sdesc_k_sw128(st + 2 * kTokBox + boff), idesc, 1u);
+                        const uint32_t acc_flag = (kc > k0 || j > 0) ? 1u : 0u;
+                        if (kCat) {
+                            const uint32_t boff = (j >> 2) * 2 * kTokBox + (j & 3) * 32;
+                            mma_f16_ts(d_tmem, a_tmem + j * 8, sdesc_k_sw128(st + boff), idesc,
+                                       acc_flag);
+                        } else {
+                            const uint32_t boff = (j >> 2) * kTokBox + (j & 3) * 32;
+                            mma_f16_ts(d_tmem, a_tmem + j * 8, sdesc_k_sw128(st + boff), idesc,
+                                       acc_flag);
+                            if (KIND == MOE_PACK_W2)
+                                mma_f16_ts(d_tmem, a_tmem + j * 8,
+                                           sdesc_k_sw128(st + 2 * kTokBox + boff), idesc, 1u);
+                        }
                     }
-                    tc_commit(&sm->empty[s]);
-                    tc_commit(&sm->a_empty[b]);
+                    // one commit frees both the stage and its A buffer
+                    tc_commit(&sm->consumed[s]);
                 }
                 if (!ok) break;
                 tc_commit(&sm->acc_full[acc]);
@@ -316,9 +337,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = (warp & 3) * 32 + lane;  // weight row of the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         for (int c = grp; c < my_chunks; c += kDqGroups) {
-            const int s = c % STAGES, b = c % kABufs;
+            const int s = c % STAGES, b = c % kAB;
             if (!warp_wait_bar(&sm->full[s], (c / STAGES) & 1, sm, a.ctrl, 4)) break;
-            if (!warp_wait_bar(&sm->a_empty[b], ((c / kABufs) & 1) ^ 1, sm, a.ctrl, 5)) break;
+            // A buffer b was last read by the MMAs of chunk c - kAB
+            if (c >= kAB) {
+                const int cp = c - kAB;
+                if (!warp_wait_bar(&sm->consumed[cp % STAGES], (cp / STAGES) & 1, sm, a.ctrl, 5)) break;
+            }
             tc_fence_after();
             const uint8_t *st = base + s * kStageBytes + kTokBoxes * kTokBox;
             const uint2 sc = *reinterpret_cast<const uint2 *>(st + kCodeBlockBytes + r * 8);
@@ -359,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int acc = seg & 1;
             if (!warp_wait_bar(&sm->acc_full[acc], (seg >> 1) & 1, sm, a.ctrl, 6)) break;
             tc_fence_after();
-            const uint32_t acc_addr = tb + lane_off + kAccBase + acc * NT;
+            const uint32_t acc_addr = tb + lane_off + kAccBase + acc * kAccCols;
             const bool whole = (k0 == 0 && k1 == KC);
             const int which = (u == u_begin) ? 0 : 1;  // first or last segment of this CTA
             float *slot = part + ((size_t)g * 2 + which) * (size_t)NT * kTileRows;
@@ -367,7 +392,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c0 = 0; c0 < t.rows; c0 += 16) {
                 uint32_t v[16];
                 tmem_ld16(acc_addr + c0, v);
-                tc_wait_ld();
+                if (kCat) {  // add the lo half, NT columns further on
+                    uint32_t lo[16];
+                    tmem_ld16(acc_addr + NT + c0, lo);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(lo[j]));
+                } else {
+                    tc_wait_ld();
+                }
                 if (whole) {
                     {
                         if (KIND == MOE_PACK_W13) {
@@ -479,7 +513,13 @@ struct Config {
     static constexpr int kFit = (kBudget / kStage) < kMaxStages ? (kBudget / kStage) : kMaxStages;
     static constexpr int kStages = kFit & ~1;
     static_assert(kStages >= 2 && kStages % kDqGroups == 0, "stage count must be a multiple of the dequant groups");
-    static constexpr size_t kSmem = (size_t)kStages * kStage + sizeof(Smem) + 1024;
+    // The kernel is persistent with one CTA per SM and allocates all of
+    // tensor memory: asking for more than half of an SM's shared memory
+    // keeps the scheduler from ever placing two of its CTAs on one SM (the
+    // second would stall in tcgen05.alloc until the first finished).
+    static constexpr size_t kMinSmem = 120 * 1024;
+    static constexpr size_t kNeed = (size_t)kStages * kStage + sizeof(Smem) + 1024;
+    static constexpr size_t kSmem = kNeed > kMinSmem ? kNeed : kMinSmem;
     static KernelFn fn() { return gemm_tc_kernel<KIND, NT, kStages>; }
 };
 

@@ -7,7 +7,7 @@
 
 namespace moe {
 
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 16;
 
 struct TcArgs {
     const uint8_t *w_codes;      // prepacked codes (header included)
