@@ -231,21 +231,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int my_chunks = (int)(u_end - u_begin);
 
     if (warp == kProducerWarp) {
-        // ---------------- TMA producer
-        if (lane == 0) {
-            pdl_wait();  // token rows come from the previous kernel
-            int c = 0;
+        // ---------------- TMA producer (the whole warp runs the loop, one
+        // elected lane issues; a converged warp keeps the loop's values in
+        // uniform registers, which the copy and MMA instructions want)
+        pdl_wait();  // token rows come from the previous kernel
+        int c = 0;
+        for (int64_t u = u_begin; u < u_end;) {
+            const int tile = (int)(u / KC), k0 = (int)(u % KC);
+            const int k1 = (int)min((int64_t)KC, k0 + (u_end - u));
+            const Tile t = decode_tile<NT>(a, tile);
             bool ok = true;
-            for (int64_t u = u_begin; u < u_end && ok;) {
-                const int tile = (int)(u / KC), k0 = (int)(u % KC);
-                const int k1 = (int)min((int64_t)KC, k0 + (u_end - u));
-                const Tile t = decode_tile<NT>(a, tile);
-                for (int kc = k0; kc < k1; ++kc, ++c) {
-                    const int s = c % STAGES;
-                    if (!wait_bar(&sm->consumed[s], ((c / STAGES) & 1) ^ 1, sm, a.ctrl, 1)) {
-                        ok = false;
-                        break;
-                    }
+            for (int kc = k0; kc < k1; ++kc, ++c) {
+                const int s = c % STAGES;
+                if (!warp_wait_bar(&sm->consumed[s], ((c / STAGES) & 1) ^ 1, sm, a.ctrl, 1)) {
+                    ok = false;
+                    break;
+                }
+                if (elect_one()) {
                     uint8_t *st = base + s * kStageBytes;
                     mbar_arrive_expect_tx(&sm->full[s], kStageBytes);
                     const int64_t blk = ((int64_t)t.e * R + t.rt) * KC + kc;
@@ -271,39 +273,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_2d(st + 3 * kTokBox, &tok_lo, x0 + 64, t.p0, &sm->full[s]);
                     }
                 }
-                u += k1 - k0;
+                __syncwarp();
             }
-            // Before the CTA exits, every copy this thread issued must have
-            // landed; after an abort elsewhere some were never consumed.  The
-            // last copy into each stage is the only one that can be pending.
-            const int issued = c;
-            for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j)
-                wait_bar_final(&sm->full[j % STAGES], (j / STAGES) & 1);
+            if (!ok) break;
+            u += k1 - k0;
         }
+        // Before the CTA exits, every copy issued must have landed; after an
+        // abort elsewhere some were never consumed.  The last copy into each
+        // stage is the only one that can be pending.
+        const int issued = c;
+        for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j)
+            wait_bar_final(&sm->full[j % STAGES], (j / STAGES) & 1);
+        __syncwarp();
     } else if (warp == kMmaWarp) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
-            int c = 0, seg = 0;
-            bool ok = true;
-            for (int64_t u = u_begin; u < u_end && ok; ++seg) {
-                const int tile = (int)(u / KC), k0 = (int)(u % KC);
-                const int k1 = (int)min((int64_t)KC, k0 + (u_end - u));
-                const Tile t = decode_tile<NT>(a, tile);
-                const int n_mma = kCat ? 2 * NT : max(16, (t.rows + 15) & ~15);
-                const uint32_t idesc = idesc_f16_m128((uint32_t)n_mma);
-                const int acc = seg & 1;
-                if (!wait_bar(&sm->acc_empty[acc], ((seg >> 1) & 1) ^ 1, sm, a.ctrl, 2)) break;
+        // ---------------- MMA issuer (converged warp, one elected lane
+        // issues; the same lane every time, so its commits track its MMAs)
+        int c = 0, seg = 0;
+        bool ok = true;
+        for (int64_t u = u_begin; u < u_end && ok; ++seg) {
+            const int tile = (int)(u / KC), k0 = (int)(u % KC);
+            const int k1 = (int)min((int64_t)KC, k0 + (u_end - u));
+            const Tile t = decode_tile<NT>(a, tile);
+            const int n_mma = kCat ? 2 * NT : max(16, (t.rows + 15) & ~15);
+            const uint32_t idesc = idesc_f16_m128((uint32_t)n_mma);
+            const int acc = seg & 1;
+            if (!warp_wait_bar(&sm->acc_empty[acc], ((seg >> 1) & 1) ^ 1, sm, a.ctrl, 2)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tb + kAccBase + acc * kAccCols;
+            for (int kc = k0; kc < k1; ++kc, ++c) {
+                const int s = c % STAGES, b = c % kAB;
+                if (!warp_wait_bar(&sm->a_full[b], (c / kAB) & 1, sm, a.ctrl, 3)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                const uint32_t d_tmem = tb + kAccBase + acc * kAccCols;
-                for (int kc = k0; kc < k1; ++kc, ++c) {
-                    const int s = c % STAGES, b = c % kAB;
-                    if (!wait_bar(&sm->a_full[b], (c / kAB) & 1, sm, a.ctrl, 3)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t st = smem_u32(base + s * kStageBytes);
-                    const uint32_t a_tmem = tb + b * kACols;
+                const uint32_t st = smem_u32(base + s * kStageBytes);
+                const uint32_t a_tmem = tb + b * kACols;
+                if (elect_one()) {
 #pragma unroll
                     for (int j = 0; j < kChunkK / 16; ++j) {
                         const uint32_t acc_flag = (kc > k0 || j > 0) ? 1u : 0u;
@@ -323,14 +329,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // one commit frees both the stage and its A buffer
                     tc_commit(&sm->consumed[s]);
                 }
-                if (!ok) break;
-                tc_commit(&sm->acc_full[acc]);
-                u += k1 - k0;
+                __syncwarp();
             }
-            // Every MMA this thread issued has completed once `done` fires.
+            if (!ok) break;
+            if (elect_one()) tc_commit(&sm->acc_full[acc]);
+            __syncwarp();
+            u += k1 - k0;
+        }
+        // Every MMA issued has completed once `done` fires.
+        if (elect_one()) {
             tc_commit(&sm->done);
             wait_bar_final(&sm->done, 0);
         }
+        __syncwarp();
     } else if (warp >= kEpiWarps) {
         // ---------------- dequantisation warpgroups
         const int grp = (warp - kEpiWarps) / 4;
