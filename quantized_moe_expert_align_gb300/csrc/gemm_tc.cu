@@ -65,6 +65,10 @@ struct Smem {
     uint32_t tmem_base;
     int abort;
     int bad;
+    // per-expert token-tile prefix and sorted-row offsets, copied once so
+    // that decoding a tile is a search in shared, not global, memory
+    int32_t tile_prefix[1025];
+    int32_t offsets[1025];
 };
 
 // Bounded wait that also gives up as soon as another role has aborted.  The
@@ -126,16 +130,22 @@ struct Tile {
 };
 
 template <int NT>
-__device__ __forceinline__ Tile decode_tile(const TcArgs &a, int tile) {
+__device__ __forceinline__ Tile decode_tile(const TcArgs &a, const Smem *sm, int tile) {
     Tile t;
     const int R = a.N / kTileRows;
-    t.e = find_segment(a.tile_prefix, a.E, tile / R);
-    const int tp0 = __ldg(a.tile_prefix + t.e), tp1 = __ldg(a.tile_prefix + t.e + 1);
+    const int v = tile / R;
+    int lo = 0, hi = a.E;  // largest e with tile_prefix[e] <= v (tile_prefix[E] > v)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (sm->tile_prefix[mid] <= v) lo = mid; else hi = mid;
+    }
+    t.e = lo;
+    const int tp0 = sm->tile_prefix[lo], tp1 = sm->tile_prefix[lo + 1];
     const int local = tile - R * tp0, te = tp1 - tp0;
     t.rt = local / te;
     const int tt = local % te;
-    t.p0 = __ldg(a.offsets + t.e) + tt * NT;
-    t.rows = min(NT, __ldg(a.offsets + t.e + 1) - t.p0);
+    t.p0 = sm->offsets[lo] + tt * NT;
+    t.rows = min(NT, sm->offsets[lo + 1] - t.p0);
     return t;
 }
 
@@ -216,6 +226,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (sm->bad && g == 0) set_status(a.ctrl, MOE_ERR_BAD_LAYOUT, KIND);
         fence_barrier_init();
     }
+    for (int i = tid; i <= a.E; i += kThreads) {
+        sm->tile_prefix[i] = __ldg(a.tile_prefix + i);
+        sm->offsets[i] = __ldg(a.offsets + i);
+    }
     if (warp == kProducerWarp && lane == 0) {
         prefetch_tensormap(&tok_hi);
         if (KIND == MOE_PACK_W2) prefetch_tensormap(&tok_lo);
@@ -226,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_trigger();
 
     const uint32_t tb = sm->tmem_base;
-    const int64_t W = sm->bad ? 0 : (int64_t)__ldg(a.tile_prefix + a.E) * R * KC;
+    const int64_t W = sm->bad ? 0 : (int64_t)sm->tile_prefix[a.E] * R * KC;
     const int64_t u_begin = range_begin(g, W, G), u_end = range_begin(g + 1, W, G);
     const int my_chunks = (int)(u_end - u_begin);
 
@@ -239,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t u = u_begin; u < u_end;) {
             const int tile = (int)(u / KC), k0 = (int)(u % KC);
             const int k1 = (int)min((int64_t)KC, k0 + (u_end - u));
-            const Tile t = decode_tile<NT>(a, tile);
+            const Tile t = decode_tile<NT>(a, sm, tile);
             bool ok = true;
             for (int kc = k0; kc < k1; ++kc, ++c) {
                 const int s = c % STAGES;
@@ -293,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t u = u_begin; u < u_end && ok; ++seg) {
             const int tile = (int)(u / KC), k0 = (int)(u % KC);
             const int k1 = (int)min((int64_t)KC, k0 + (u_end - u));
-            const Tile t = decode_tile<NT>(a, tile);
+            const Tile t = decode_tile<NT>(a, sm, tile);
             const int n_mma = kCat ? 2 * NT : max(16, (t.rows + 15) & ~15);
             const uint32_t idesc = idesc_f16_m128((uint32_t)n_mma);
             const int acc = seg & 1;
@@ -307,7 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t st = smem_u32(base + s * kStageBytes);
+                // descriptor of the stage's first K slice; a byte offset of
+                // the start address adds offset >> 4 to the descriptor
+                const uint64_t desc0 = sdesc_k_sw128(smem_u32(base + s * kStageBytes));
                 const uint32_t a_tmem = tb + b * kACols;
                 if (elect_one()) {
 #pragma unroll
@@ -315,15 +331,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t acc_flag = (kc > k0 || j > 0) ? 1u : 0u;
                         if (kCat) {
                             const uint32_t boff = (j >> 2) * 2 * kTokBox + (j & 3) * 32;
-                            mma_f16_ts(d_tmem, a_tmem + j * 8, sdesc_k_sw128(st + boff), idesc,
-                                       acc_flag);
+                            mma_f16_ts(d_tmem, a_tmem + j * 8, desc0 + (boff >> 4), idesc, acc_flag);
                         } else {
                             const uint32_t boff = (j >> 2) * kTokBox + (j & 3) * 32;
-                            mma_f16_ts(d_tmem, a_tmem + j * 8, sdesc_k_sw128(st + boff), idesc,
-                                       acc_flag);
+                            mma_f16_ts(d_tmem, a_tmem + j * 8, desc0 + (boff >> 4), idesc, acc_flag);
                             if (KIND == MOE_PACK_W2)
                                 mma_f16_ts(d_tmem, a_tmem + j * 8,
-                                           sdesc_k_sw128(st + 2 * kTokBox + boff), idesc, 1u);
+                                           desc0 + ((2 * kTokBox + boff) >> 4), idesc, 1u);
                         }
                     }
                     // one commit frees both the stage and its A buffer
@@ -357,12 +371,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint8_t *st = base + s * kStageBytes + kTokBoxes * kTokBox;
-            const uint2 sc = *reinterpret_cast<const uint2 *>(st + kCodeBlockBytes + r * 8);
+            const uint32_t st_s = smem_u32(st);
+            uint2 sc;
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                         : "=r"(sc.x), "=r"(sc.y) : "r"(st_s + kCodeBlockBytes + r * 8));
             const uint32_t scw[2] = {sc.x, sc.y};
             const uint32_t a_addr = tb + lane_off + b * kACols;
 #pragma unroll
             for (int pc = 0; pc < 4; ++pc) {
-                const uint4 q = *reinterpret_cast<const uint4 *>(st + (pc * kTileRows + r) * 16);
+                uint4 q;
+                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w)
+                             : "r"(st_s + (pc * kTileRows + r) * 16));
                 const uint32_t sbits = (scw[pc >> 1] >> ((pc & 1) * 16)) & 0xFFFFu;
                 const __half hs = __ushort_as_half((unsigned short)sbits);
                 const __half2 s2 = __halves2half2(hs, hs);
@@ -391,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t u = u_begin; u < u_end; ++seg) {
             const int tile = (int)(u / KC), k0 = (int)(u % KC);
             const int k1 = (int)min((int64_t)KC, k0 + (u_end - u));
-            const Tile t = decode_tile<NT>(a, tile);
+            const Tile t = decode_tile<NT>(a, sm, tile);
             const int acc = seg & 1;
             if (!warp_wait_bar(&sm->acc_full[acc], (seg >> 1) & 1, sm, a.ctrl, 6)) break;
             tc_fence_after();
