@@ -233,7 +233,7 @@ def our_arm(args, wl):
 
     def call(M):
         x, ids, w, out = devb[M]
-        st = moe.moe_w4a16_forward(x, ids, w, p13[0], p13[1], p2[0], p2[1], out, M, L.k, L.E,
+        st = moe.moe_w4a16_forward(x, ids, w, p13, p2, out, M, L.k, L.E,
                                    L.H, L.I, ws.buf, stream)
         if st != moe.MOE_OK:
             raise moe.MoeError(st, "moe_w4a16_forward")
@@ -292,7 +292,7 @@ def our_arm(args, wl):
             x, ids, w, out = devb[M]
             evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
             flush.zero_()
-            st = moe.moe_w4a16_forward_profiled(x, ids, w, p13[0], p13[1], p2[0], p2[1], out, M,
+            st = moe.moe_w4a16_forward_profiled(x, ids, w, p13, p2, out, M,
                                                 L.k, L.E, L.H, L.I, ws.buf, evs, stream)
             if st != moe.MOE_OK:
                 raise moe.MoeError(st, "moe_w4a16_forward_profiled")

@@ -72,13 +72,13 @@ typedef enum {
 const char *moe_status_string(moe_status_t status);
 
 /*
- * Bytes of the two prepacked buffers for one matrix: the packed codes and
- * the scales, each with a 256-byte header.  Requires group == 32,
- * N % 128 == 0, K % 128 == 0, E >= 1; otherwise returns MOE_ERR_INVALID_ARG
- * and sets both sizes to 0.
+ * Bytes of the prepacked buffer for one matrix: a 256-byte header, then
+ * 9 KiB per (expert, 128-row tile, 128-element K chunk).  Requires
+ * group == 32, N % 128 == 0, K % 128 == 0, E >= 1; otherwise returns
+ * MOE_ERR_INVALID_ARG and sets *bytes to 0.
  */
-moe_status_t moe_w4a16_prepack_sizes(int kind, int E, int N, int K, int group,
-                                     size_t *code_bytes, size_t *scale_bytes);
+moe_status_t moe_w4a16_prepack_size(int kind, int E, int N, int K, int group,
+                                    size_t *bytes);
 
 /*
  * Repack canonical weights into the library's layout (done once per layer at
@@ -89,22 +89,22 @@ moe_status_t moe_w4a16_prepack_sizes(int kind, int E, int N, int K, int group,
  *  q_canon [E][N][K/2] uint8, device: element kk of row n sits in byte kk/2,
  *          in the low nibble when kk is even, the high nibble when odd.
  *  scales  [E][N][K/32] bf16 bit patterns, device.
- *  code_dst / scale_dst: device buffers of at least the sizes given by
- *          moe_w4a16_prepack_sizes, 256-byte aligned.
+ *  dst     device buffer of at least moe_w4a16_prepack_size bytes,
+ *          256-byte aligned; the caller owns it.
  * Layout written: per expert, 128-row tiles (for w13 each tile holds 64 gate
  * rows interleaved with the 64 matching up rows), per 128-element K chunk one
- * 8 KiB code block and one 1 KiB scale block, codes reordered for a cheap
- * 4-bit -> fp16 conversion and scales stored as fp16.
+ * 9 KiB block: 8 KiB of codes, reordered for a cheap 4-bit -> fp16
+ * conversion, followed by the chunk's 1 KiB of scales as fp16, so that one
+ * contiguous copy brings a chunk's weights on chip.
  *
  * Every scale must be zero, NaN, infinite or of magnitude in
  * [2^-14, 8188] so that every (q - 8) * scale is exact in fp16; otherwise the
- * call returns MOE_ERR_DEVICE_FP16_RANGE and marks the buffers invalid.
+ * call returns MOE_ERR_DEVICE_FP16_RANGE and marks the buffer invalid.
  * This call waits for its own work on `stream` to finish.
  */
 moe_status_t moe_w4a16_prepack(int kind, const uint8_t *q_canon,
                                const uint16_t *scales, int E, int N, int K,
-                               int group, void *code_dst, size_t code_bytes,
-                               void *scale_dst, size_t scale_bytes,
+                               int group, void *dst, size_t dst_bytes,
                                moe_stream_t stream);
 
 /* Workspace bytes needed by moe_align (256-byte aligned buffer). */
@@ -139,8 +139,8 @@ size_t moe_w4a16_workspace_size(int M, int k, int E, int H, int I);
  * MoE layer forward.
  *  hidden [M][H] bf16, device, 16-byte aligned.
  *  topk_ids [M][k] int32, topk_w [M][k] fp32 (used as given), device.
- *  w13/s13: prepacked gate+up codes/scales (kind MOE_PACK_W13, N = 2I, K = H)
- *  w2/s2:   prepacked down codes/scales   (kind MOE_PACK_W2,  N = H,  K = I)
+ *  w13: prepacked gate+up weights (kind MOE_PACK_W13, N = 2I, K = H)
+ *  w2:  prepacked down weights    (kind MOE_PACK_W2,  N = H,  K = I)
  *  out [M][H] bf16, device, 16-byte aligned: written once, rounded to
  *           nearest-even from an fp32 combine over ascending slots.
  *  workspace: moe_w4a16_workspace_size(...) bytes, 256-byte aligned.
@@ -155,8 +155,7 @@ size_t moe_w4a16_workspace_size(int M, int k, int E, int H, int I);
  * accumulation, the activation passed to the down GEMM as an fp16 hi+lo pair.
  */
 moe_status_t moe_w4a16_forward(const uint16_t *hidden, const int32_t *topk_ids,
-                               const float *topk_w, const void *w13,
-                               const void *s13, const void *w2, const void *s2,
+                               const float *topk_w, const void *w13, const void *w2,
                                uint16_t *out, int M, int k, int E, int H, int I,
                                void *workspace, size_t ws_bytes,
                                moe_stream_t stream);
@@ -172,8 +171,7 @@ moe_status_t moe_w4a16_forward(const uint16_t *hidden, const int32_t *topk_ids,
  * MOE_ERR_INVALID_ARG if events is NULL or n_events < 6.
  */
 moe_status_t moe_w4a16_forward_profiled(const uint16_t *hidden, const int32_t *topk_ids,
-                                        const float *topk_w, const void *w13,
-                                        const void *s13, const void *w2, const void *s2,
+                                        const float *topk_w, const void *w13, const void *w2,
                                         uint16_t *out, int M, int k, int E, int H, int I,
                                         void *workspace, size_t ws_bytes,
                                         moe_stream_t stream, void **events, int n_events);
@@ -213,9 +211,9 @@ moe_status_t moe_w4a16_forward_profiled(const uint16_t *hidden, const int32_t *t
  *    workspace when those errors must be observed.
  */
 moe_status_t moe_w4a16_forward_static(const uint16_t *hidden, const int32_t *topk_ids,
-                                      const float *topk_w, const void *w13, const void *s13,
-                                      const void *w2, const void *s2, uint16_t *out, int M,
-                                      int k, int E, int H, int I, moe_stream_t stream);
+                                      const float *topk_w, const void *w13, const void *w2,
+                                      uint16_t *out, int M, int k, int E, int H, int I,
+                                      moe_stream_t stream);
 
 /*
  * Wait for `stream`, then return the status word the device recorded in

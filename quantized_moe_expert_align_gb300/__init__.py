@@ -67,15 +67,15 @@ def load(path: str = LIB_PATH):
         i, p, sz = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
         sig = {
             "moe_status_string": (ctypes.c_char_p, [i]),
-            "moe_w4a16_prepack_sizes": (i, [i, i, i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
-            "moe_w4a16_prepack": (i, [i, p, p, i, i, i, i, p, sz, p, sz, p]),
+            "moe_w4a16_prepack_size": (i, [i, i, i, i, i, ctypes.POINTER(sz)]),
+            "moe_w4a16_prepack": (i, [i, p, p, i, i, i, i, p, sz, p]),
             "moe_align_workspace_size": (sz, [i, i, i]),
             "moe_align": (i, [p, i, i, i, p, p, p, p, p, sz, p]),
             "moe_w4a16_workspace_size": (sz, [i, i, i, i, i]),
-            "moe_w4a16_forward": (i, [p, p, p, p, p, p, p, p, i, i, i, i, i, p, sz, p]),
-            "moe_w4a16_forward_profiled": (i, [p, p, p, p, p, p, p, p, i, i, i, i, i, p, sz, p,
+            "moe_w4a16_forward": (i, [p, p, p, p, p, p, i, i, i, i, i, p, sz, p]),
+            "moe_w4a16_forward_profiled": (i, [p, p, p, p, p, p, i, i, i, i, i, p, sz, p,
                                                ctypes.POINTER(p), i]),
-            "moe_w4a16_forward_static": (i, [p, p, p, p, p, p, p, p, i, i, i, i, i, p]),
+            "moe_w4a16_forward_static": (i, [p, p, p, p, p, p, i, i, i, i, i, p]),
             "moe_w4a16_get_device_status": (i, [p, p, ctypes.POINTER(ctypes.c_int32)]),
             "moe_w4a16_get_diag": (i, [ctypes.POINTER(moe_diag_t)]),
             "moe_w4a16_workspace_views": (i, [i, i, i, i, i, ctypes.POINTER(moe_ws_views_t)]),
@@ -107,17 +107,15 @@ def moe_status_string(status: int) -> str:
     return load().moe_status_string(status).decode()
 
 
-def moe_w4a16_prepack_sizes(kind, E, N, K, group=32):
-    c, s = ctypes.c_size_t(0), ctypes.c_size_t(0)
-    st = load().moe_w4a16_prepack_sizes(kind, E, N, K, group, ctypes.byref(c), ctypes.byref(s))
-    return st, c.value, s.value
+def moe_w4a16_prepack_size(kind, E, N, K, group=32):
+    b = ctypes.c_size_t(0)
+    st = load().moe_w4a16_prepack_size(kind, E, N, K, group, ctypes.byref(b))
+    return st, b.value
 
 
-def moe_w4a16_prepack(kind, q_canon, scales, E, N, K, group, code_dst, scale_dst, stream=None):
+def moe_w4a16_prepack(kind, q_canon, scales, E, N, K, group, dst, stream=None):
     return load().moe_w4a16_prepack(kind, _p(q_canon), _p(scales), E, N, K, group,
-                                    _p(code_dst), code_dst.numel() * code_dst.element_size(),
-                                    _p(scale_dst), scale_dst.numel() * scale_dst.element_size(),
-                                    _stream(stream))
+                                    _p(dst), dst.numel() * dst.element_size(), _stream(stream))
 
 
 def moe_align_workspace_size(M, k, E):
@@ -134,14 +132,14 @@ def moe_w4a16_workspace_size(M, k, E, H, I):
     return load().moe_w4a16_workspace_size(M, k, E, H, I)
 
 
-def moe_w4a16_forward(hidden, topk_ids, topk_w, w13, s13, w2, s2, out, M, k, E, H, I,
-                      workspace, stream=None):
-    return load().moe_w4a16_forward(_p(hidden), _p(topk_ids), _p(topk_w), _p(w13), _p(s13),
-                                    _p(w2), _p(s2), _p(out), M, k, E, H, I, _p(workspace),
+def moe_w4a16_forward(hidden, topk_ids, topk_w, w13, w2, out, M, k, E, H, I, workspace,
+                      stream=None):
+    return load().moe_w4a16_forward(_p(hidden), _p(topk_ids), _p(topk_w), _p(w13), _p(w2),
+                                    _p(out), M, k, E, H, I, _p(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream))
 
 
-def moe_w4a16_forward_profiled(hidden, topk_ids, topk_w, w13, s13, w2, s2, out, M, k, E, H, I,
+def moe_w4a16_forward_profiled(hidden, topk_ids, topk_w, w13, w2, out, M, k, E, H, I,
                                workspace, events, stream=None):
     """``events``: six torch.cuda.Event(enable_timing=True) objects."""
     for e in events:
@@ -149,16 +147,16 @@ def moe_w4a16_forward_profiled(hidden, topk_ids, topk_w, w13, s13, w2, s2, out, 
             e.record()
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     return load().moe_w4a16_forward_profiled(
-        _p(hidden), _p(topk_ids), _p(topk_w), _p(w13), _p(s13), _p(w2), _p(s2), _p(out), M, k, E,
-        H, I, _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream), arr,
+        _p(hidden), _p(topk_ids), _p(topk_w), _p(w13), _p(w2), _p(out), M, k, E, H, I,
+        _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream), arr,
         len(events))
 
 
-def moe_w4a16_forward_static(hidden, topk_ids, topk_w, w13, s13, w2, s2, out, M, k, E, H, I,
+def moe_w4a16_forward_static(hidden, topk_ids, topk_w, w13, w2, out, M, k, E, H, I,
                              stream=None):
     """The forward on the library's static device scratch (no workspace)."""
-    return load().moe_w4a16_forward_static(_p(hidden), _p(topk_ids), _p(topk_w), _p(w13), _p(s13),
-                                           _p(w2), _p(s2), _p(out), M, k, E, H, I, _stream(stream))
+    return load().moe_w4a16_forward_static(_p(hidden), _p(topk_ids), _p(topk_w), _p(w13), _p(w2),
+                                           _p(out), M, k, E, H, I, _stream(stream))
 
 
 MOE_W4A16_STATIC_SCRATCH_BYTES = 16 << 20
@@ -227,19 +225,19 @@ def _empty_bytes(nbytes, device):
 
 def prepack(kind, q_canon, scales, stream=None):
     """Prepack canonical codes [E][N][K/2] (uint8) and bf16 scales [E][N][K/32]
-    (int16/uint16/bfloat16 bits) that live on the GPU; returns (codes, scales)."""
+    (int16/uint16/bfloat16 bits) that live on the GPU; returns the packed
+    uint8 buffer."""
     import torch
     E, N, half = q_canon.shape
     K = half * 2
-    st, cb, sb = moe_w4a16_prepack_sizes(kind, E, N, K, 32)
-    _check(st, "moe_w4a16_prepack_sizes")
-    codes = _empty_bytes(cb, q_canon.device)
-    sc = _empty_bytes(sb, q_canon.device)
+    st, nb = moe_w4a16_prepack_size(kind, E, N, K, 32)
+    _check(st, "moe_w4a16_prepack_size")
+    packed = _empty_bytes(nb, q_canon.device)
     if scales.dtype == torch.bfloat16:
         scales = scales.view(torch.int16)
     _check(moe_w4a16_prepack(kind, q_canon.contiguous(), scales.contiguous(), E, N, K, 32,
-                             codes, sc, stream), "moe_w4a16_prepack")
-    return codes, sc
+                             packed, stream), "moe_w4a16_prepack")
+    return packed
 
 
 def align(topk_ids, E, stream=None):
@@ -267,8 +265,7 @@ class Workspace:
         self.buf = _empty_bytes(self.nbytes, device)
 
 
-def forward(hidden, topk_ids, topk_w, w13, s13, w2, s2, E, I, out=None, workspace=None,
-            stream=None):
+def forward(hidden, topk_ids, topk_w, w13, w2, E, I, out=None, workspace=None, stream=None):
     """out[M][H] bf16 = MoE layer forward; raises MoeError on a host-side error."""
     import torch
     M, H = hidden.shape
@@ -278,6 +275,6 @@ def forward(hidden, topk_ids, topk_w, w13, s13, w2, s2, E, I, out=None, workspac
     ws = workspace.buf if isinstance(workspace, Workspace) else workspace
     if ws is None:
         ws = Workspace(M, k, E, H, I, hidden.device).buf
-    _check(moe_w4a16_forward(hidden, topk_ids, topk_w, w13, s13, w2, s2, out, M, k, E, H, I, ws,
-                             stream), "moe_w4a16_forward")
+    _check(moe_w4a16_forward(hidden, topk_ids, topk_w, w13, w2, out, M, k, E, H, I, ws, stream),
+           "moe_w4a16_forward")
     return out

@@ -121,52 +121,47 @@ const char *moe_status_string(moe_status_t s) {
     return "MOE_ERR_UNKNOWN";
 }
 
-moe_status_t moe_w4a16_prepack_sizes(int kind, int E, int N, int K, int group,
-                                     size_t *code_b, size_t *scale_b) {
-    if (code_b) *code_b = 0;
-    if (scale_b) *scale_b = 0;
-    if (!code_b || !scale_b) return MOE_ERR_INVALID_ARG;
+moe_status_t moe_w4a16_prepack_size(int kind, int E, int N, int K, int group, size_t *bytes) {
+    if (bytes) *bytes = 0;
+    if (!bytes) return MOE_ERR_INVALID_ARG;
     if ((kind != MOE_PACK_W13 && kind != MOE_PACK_W2) || group != kGroup || E < 1 || N <= 0 ||
         K <= 0 || N % kTileRows || K % kChunkK || N > (1 << 20) || K > (1 << 20))
         return MOE_ERR_INVALID_ARG;
-    *code_b = code_bytes(E, N, K);
-    *scale_b = scale_bytes(E, N, K);
+    *bytes = packed_bytes(E, N, K);
     return MOE_OK;
 }
 
 moe_status_t moe_w4a16_prepack(int kind, const uint8_t *q_canon, const uint16_t *scales, int E,
-                               int N, int K, int group, void *code_dst, size_t code_b,
-                               void *scale_dst, size_t scale_b, moe_stream_t stream) {
-    size_t need_c = 0, need_s = 0;
-    moe_status_t st = moe_w4a16_prepack_sizes(kind, E, N, K, group, &need_c, &need_s);
+                               int N, int K, int group, void *dst, size_t dst_bytes,
+                               moe_stream_t stream) {
+    size_t need = 0;
+    moe_status_t st = moe_w4a16_prepack_size(kind, E, N, K, group, &need);
     if (st != MOE_OK) return st;
-    if (!q_canon || !scales || !code_dst || !scale_dst) return MOE_ERR_INVALID_ARG;
-    if (!aligned(q_canon, 16) || !aligned(scales, 16) || !aligned(code_dst, 256) ||
-        !aligned(scale_dst, 256))
+    if (!q_canon || !scales || !dst) return MOE_ERR_INVALID_ARG;
+    if (!aligned(q_canon, 16) || !aligned(scales, 16) || !aligned(dst, 256))
         return MOE_ERR_MISALIGNED;
-    if (code_b < need_c || scale_b < need_s) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if (dst_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
     if ((st = check_device()) != MOE_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-    PackHeader hc;
-    std::memset(&hc, 0, sizeof hc);
-    hc.magic = kPackMagic;
-    hc.version = kPackVersion;
-    hc.kind = (uint32_t)kind;
-    hc.part = kPartCodes;
-    hc.E = E;
-    hc.N = N;
-    hc.K = K;
-    hc.group = group;
-    hc.status = MOE_OK;
-    PackHeader hs = hc;
-    hs.part = kPartScales;
-    uint8_t *cd = static_cast<uint8_t *>(code_dst), *sd = static_cast<uint8_t *>(scale_dst);
-    int32_t *flag = &reinterpret_cast<PackHeader *>(sd)->status;
-    if (cudaMemcpyAsync(cd, &hc, sizeof hc, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(sd, &hs, sizeof hs, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        launch_prepack_codes(kind, q_canon, E, N, K, cd, s) != cudaSuccess ||
-        launch_prepack_scales(kind, scales, E, N, K, sd, flag, s) != cudaSuccess ||
+    PackHeader h;
+    std::memset(&h, 0, sizeof h);
+    h.magic = kPackMagic;
+    h.version = kPackVersion;
+    h.kind = (uint32_t)kind;
+    h.block_bytes = kBlockBytes;
+    h.E = E;
+    h.N = N;
+    h.K = K;
+    h.group = group;
+    h.status = MOE_OK;
+    uint8_t *d = static_cast<uint8_t *>(dst);
+    // a scale outside the exact range sets the header's status, which makes
+    // every later forward reject the buffer
+    int32_t *flag = &reinterpret_cast<PackHeader *>(d)->status;
+    if (cudaMemcpyAsync(d, &h, sizeof h, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        launch_prepack_codes(kind, q_canon, E, N, K, d, s) != cudaSuccess ||
+        launch_prepack_scales(kind, scales, E, N, K, d, flag, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;
@@ -219,15 +214,14 @@ size_t moe_w4a16_workspace_size(int M, int k, int E, int H, int I) {
 }
 
 static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, const float *topk_w,
-                                 const void *w13, const void *s13, const void *w2, const void *s2,
-                                 uint16_t *out, int M, int k, int E, int H, int I, void *workspace,
-                                 size_t ws_bytes, moe_stream_t stream, cudaEvent_t *ev) {
+                                 const void *w13, const void *w2, uint16_t *out, int M, int k,
+                                 int E, int H, int I, void *workspace, size_t ws_bytes,
+                                 moe_stream_t stream, cudaEvent_t *ev) {
     if (!layer_sizes_ok(M, k, E, H, I)) return MOE_ERR_INVALID_ARG;
-    if (!w13 || !s13 || !w2 || !s2 || !workspace) return MOE_ERR_INVALID_ARG;
+    if (!w13 || !w2 || !workspace) return MOE_ERR_INVALID_ARG;
     if (M > 0 && (!hidden || !ids || !topk_w || !out)) return MOE_ERR_INVALID_ARG;
     if (!aligned(hidden, 16) || !aligned(out, 16) || !aligned(ids, 4) || !aligned(topk_w, 4) ||
-        !aligned(w13, 256) || !aligned(s13, 256) || !aligned(w2, 256) || !aligned(s2, 256) ||
-        !aligned(workspace, 256))
+        !aligned(w13, 256) || !aligned(w2, 256) || !aligned(workspace, 256))
         return MOE_ERR_MISALIGNED;
     const FwdLayout L = fwd_layout(M, k, E, H, I);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -264,8 +258,7 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
                     tickets, r1, r2, L.max_tok_tiles * r1};
     GatherArgs ga = {hidden, perm, offsets, n, k, H, E, xs, ctrl};
     TcArgs g1 = {};
-    g1.w_codes = static_cast<const uint8_t *>(w13);
-    g1.w_scales = static_cast<const uint8_t *>(s13);
+    g1.w = static_cast<const uint8_t *>(w13);
     g1.offsets = offsets;
     g1.tile_prefix = tile_prefix;
     g1.tickets = tickets;
@@ -280,8 +273,7 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     g1.act_lo = act_lo;
     g1.ctrl = ctrl;
     TcArgs g2 = g1;
-    g2.w_codes = static_cast<const uint8_t *>(w2);
-    g2.w_scales = static_cast<const uint8_t *>(s2);
+    g2.w = static_cast<const uint8_t *>(w2);
     g2.tickets = tickets + L.max_tok_tiles * r1;
     g2.N = H;
     g2.K = I;
@@ -289,17 +281,17 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     g2.y = y;
     CombineArgs cb = {y, inv_perm, topk_w, M, k, H, out};
 
-    CUtensorMap map_x, map_hi, map_lo;
-    if (!make_token_map(&map_x, xs, n, H, L.nt) || !make_token_map(&map_hi, act_hi, n, I, L.nt) ||
-        !make_token_map(&map_lo, act_lo, n, I, L.nt))
+    CUtensorMap map_x, map_act;
+    if (!make_token_map(&map_x, xs, n, H, L.nt) ||
+        !make_act_map(&map_act, act_hi, act_lo, n, I, L.nt, stacked_hi_lo(L.nt)))
         return MOE_ERR_CUDA;
 
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
     const bool pdl = (ev == nullptr);
     if (mark(0) != cudaSuccess || launch_align(al, s) != cudaSuccess || mark(1) != cudaSuccess ||
         launch_gather_hidden(ga, s, pdl) != cudaSuccess || mark(2) != cudaSuccess ||
-        launch_gemm_tc(g1, map_x, map_x, grid, s, pdl) != cudaSuccess || mark(3) != cudaSuccess ||
-        launch_gemm_tc(g2, map_hi, map_lo, grid, s, pdl) != cudaSuccess || mark(4) != cudaSuccess ||
+        launch_gemm_tc(g1, map_x, grid, s, pdl) != cudaSuccess || mark(3) != cudaSuccess ||
+        launch_gemm_tc(g2, map_act, grid, s, pdl) != cudaSuccess || mark(4) != cudaSuccess ||
         launch_combine(cb, s, pdl) != cudaSuccess || mark(5) != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;
@@ -319,23 +311,22 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
 }
 
 moe_status_t moe_w4a16_forward(const uint16_t *hidden, const int32_t *ids, const float *topk_w,
-                               const void *w13, const void *s13, const void *w2, const void *s2,
+                               const void *w13, const void *w2,
                                uint16_t *out, int M, int k, int E, int H, int I, void *workspace,
                                size_t ws_bytes, moe_stream_t stream) {
-    return forward_impl(hidden, ids, topk_w, w13, s13, w2, s2, out, M, k, E, H, I, workspace,
+    return forward_impl(hidden, ids, topk_w, w13, w2, out, M, k, E, H, I, workspace,
                         ws_bytes, stream, nullptr);
 }
 
 moe_status_t moe_w4a16_forward_profiled(const uint16_t *hidden, const int32_t *ids,
-                                        const float *topk_w, const void *w13, const void *s13,
-                                        const void *w2, const void *s2, uint16_t *out, int M,
+                                        const float *topk_w, const void *w13, const void *w2, uint16_t *out, int M,
                                         int k, int E, int H, int I, void *workspace,
                                         size_t ws_bytes, moe_stream_t stream, void **events,
                                         int n_events) {
     if (!events || n_events < 6) return MOE_ERR_INVALID_ARG;
     for (int i = 0; i < 6; ++i)
         if (!events[i]) return MOE_ERR_INVALID_ARG;
-    return forward_impl(hidden, ids, topk_w, w13, s13, w2, s2, out, M, k, E, H, I, workspace,
+    return forward_impl(hidden, ids, topk_w, w13, w2, out, M, k, E, H, I, workspace,
                         ws_bytes, stream, reinterpret_cast<cudaEvent_t *>(events));
 }
 
@@ -380,10 +371,9 @@ namespace moe {
 // The forward on a caller-chosen scratch buffer (used by the entry point
 // whose scratch is a static device array).
 moe_status_t forward_on_scratch(const uint16_t *hidden, const int32_t *ids, const float *topk_w,
-                                const void *w13, const void *s13, const void *w2, const void *s2,
-                                uint16_t *out, int M, int k, int E, int H, int I, void *scratch,
+                                const void *w13, const void *w2, uint16_t *out, int M, int k, int E, int H, int I, void *scratch,
                                 size_t scratch_bytes, moe_stream_t stream) {
-    return forward_impl(hidden, ids, topk_w, w13, s13, w2, s2, out, M, k, E, H, I, scratch,
+    return forward_impl(hidden, ids, topk_w, w13, w2, out, M, k, E, H, I, scratch,
                         scratch_bytes, stream, nullptr);
 }
 

@@ -30,12 +30,11 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
 }
 
 // Validate a prepacked buffer header against the expected geometry.
-__device__ __forceinline__ bool header_ok(const uint8_t *buf, uint32_t kind, uint32_t part,
-                                          int E, int N, int K) {
+__device__ __forceinline__ bool header_ok(const uint8_t *buf, uint32_t kind, int E, int N, int K) {
     const PackHeader *h = reinterpret_cast<const PackHeader *>(buf);
     return h->magic == kPackMagic && h->version == kPackVersion && h->kind == kind &&
-           h->part == part && h->E == E && h->N == N && h->K == K && h->group == kGroup &&
-           h->status == MOE_OK;
+           h->block_bytes == (uint32_t)kBlockBytes && h->E == E && h->N == N && h->K == K &&
+           h->group == kGroup && h->status == MOE_OK;
 }
 
 // Index of the expert owning tile `tile`: the largest e with prefix[e] <= tile

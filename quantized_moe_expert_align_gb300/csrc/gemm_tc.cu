@@ -47,10 +47,11 @@ namespace {
 using namespace sm100;
 
 constexpr int kEpiWarps = 4;
-constexpr int kDqGroups = 2;
-constexpr int kThreads = 32 * (kEpiWarps + 4 * kDqGroups + 2);  // 448
-constexpr int kProducerWarp = kEpiWarps + 4 * kDqGroups;         // 12
-constexpr int kMmaWarp = kProducerWarp + 1;                      // 13
+// Warps: 4 epilogue, 4 per dequantisation warpgroup, one or two TMA
+// producers and one or two MMA issuers.
+__host__ __device__ constexpr int threads_for(int dq_groups, int producers, int mma_warps) {
+    return 32 * (kEpiWarps + 4 * dq_groups + producers + mma_warps);
+}
 constexpr int kMaxABufs = 4;                  // TMEM A buffers (64 columns each)
 constexpr int kACols = kChunkK / 2;           // 64 fp16 pairs per row per chunk
 constexpr uint32_t kTmemCols = 512;
@@ -176,24 +177,29 @@ __device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, uint32_t (&
     o[3] = *reinterpret_cast<uint32_t *>(&h3);
 }
 
-template <int KIND, int NT, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tok_hi,
-                   const __grid_constant__ CUtensorMap tok_lo) {
+template <int KIND, int NT, int STAGES, int DQG, int NPROD, int MMAW>
+__global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
+    gemm_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tok) {
+    constexpr int kDqGroups = DQG;
+    constexpr int kThreads = threads_for(DQG, NPROD, MMAW);
+    constexpr int kProducerWarp = kEpiWarps + 4 * DQG;
+    constexpr int kMmaWarp = kProducerWarp + NPROD;
     constexpr int kTokBox = NT * 128;                        // one 64-column box
     constexpr int kTokBoxes = (KIND == MOE_PACK_W2) ? 4 : 2;  // hi(+lo) x 2 boxes
-    constexpr int kStageBytes = kTokBoxes * kTokBox + kCodeBlockBytes + kScaleBlockBytes;
+    constexpr int kStageBytes = kTokBoxes * kTokBox + kBlockBytes;
     // Down GEMM with small token tiles: the hi and lo rows of a are stacked
     // into one B operand of 2*NT rows, so one MMA (whose cost does not grow
     // with N up to 128) covers both; the epilogue adds the two halves.
-    constexpr bool kCat = (KIND == MOE_PACK_W2) && (NT <= 64);
+    constexpr bool kCat = (KIND == MOE_PACK_W2) && (NT <= 64);  // == stacked_hi_lo(NT)
     constexpr int kAB = (STAGES >= 4) ? 4 : 2;               // TMEM A buffers in use
     constexpr int kAccBase = kAB * kACols;
     constexpr int kAccCols = kCat ? 2 * NT : NT;              // columns per accumulator
-    static_assert(kAccBase + 2 * kAccCols <= 512, "tensor memory budget");
+    static_assert(kAccBase + 2 * MMAW * kAccCols <= 512, "tensor memory budget");
     static_assert(STAGES >= kAB, "a stage must outlive its A buffer's reuse distance");
     static_assert(kStageBytes % 1024 == 0, "stage size must keep 1024-byte alignment");
     static_assert(STAGES % kDqGroups == 0, "each stage must belong to one dequant group");
+    static_assert(kAB % kDqGroups == 0, "each A buffer must belong to one dequant group");
+    static_assert(STAGES % NPROD == 0, "each stage must belong to one producer");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
@@ -216,13 +222,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < kAB; ++b) mbar_init(&sm->a_full[b], 128);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&sm->acc_full[b], 1);
+            mbar_init(&sm->acc_full[b], MMAW);
             mbar_init(&sm->acc_empty[b], 128);
         }
-        mbar_init(&sm->done, 1);
+        mbar_init(&sm->done, MMAW);
         sm->abort = 0;
-        sm->bad = !(header_ok(a.w_codes, KIND, kPartCodes, a.E, a.N, a.K) &&
-                    header_ok(a.w_scales, KIND, kPartScales, a.E, a.N, a.K));
+        sm->bad = !header_ok(a.w, KIND, a.E, a.N, a.K);
         if (sm->bad && g == 0) set_status(a.ctrl, MOE_ERR_BAD_LAYOUT, KIND);
         fence_barrier_init();
     }
@@ -230,10 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm->tile_prefix[i] = __ldg(a.tile_prefix + i);
         sm->offsets[i] = __ldg(a.offsets + i);
     }
-    if (warp == kProducerWarp && lane == 0) {
-        prefetch_tensormap(&tok_hi);
-        if (KIND == MOE_PACK_W2) prefetch_tensormap(&tok_lo);
-    }
+    if (warp == kProducerWarp && lane == 0) prefetch_tensormap(&tok);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -244,65 +246,86 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t u_begin = range_begin(g, W, G), u_end = range_begin(g + 1, W, G);
     const int my_chunks = (int)(u_end - u_begin);
 
-    if (warp == kProducerWarp) {
-        // ---------------- TMA producer (the whole warp runs the loop, one
+    if (warp >= kProducerWarp && warp < kMmaWarp) {
+        // ---------------- TMA producers (the whole warp runs the loop, one
         // elected lane issues; a converged warp keeps the loop's values in
-        // uniform registers, which the copy and MMA instructions want)
+        // uniform registers, which the copy and MMA instructions want).
+        // Every mbarrier wait costs a round trip of well over a hundred
+        // cycles even when the phase is already complete, so one warp
+        // alone cannot keep the HBM stream going; with two, producer pw
+        // takes the chunks c with c % 2 == pw (and thereby its own stages).
+        const int pw = warp - kProducerWarp;
         pdl_wait();  // token rows come from the previous kernel
-        int c = 0;
-        for (int64_t u = u_begin; u < u_end;) {
-            const int tile = (int)(u / KC), k0 = (int)(u % KC);
-            const int k1 = (int)min((int64_t)KC, k0 + (u_end - u));
-            const Tile t = decode_tile<NT>(a, sm, tile);
-            bool ok = true;
-            for (int kc = k0; kc < k1; ++kc, ++c) {
-                const int s = c % STAGES;
-                if (!warp_wait_bar(&sm->consumed[s], ((c / STAGES) & 1) ^ 1, sm, a.ctrl, 1)) {
-                    ok = false;
-                    break;
-                }
-                if (elect_one()) {
-                    uint8_t *st = base + s * kStageBytes;
-                    mbar_arrive_expect_tx(&sm->full[s], kStageBytes);
-                    const int64_t blk = ((int64_t)t.e * R + t.rt) * KC + kc;
-                    bulk_g2s(st + kTokBoxes * kTokBox,
-                             a.w_codes + kHeaderBytes + blk * kCodeBlockBytes, kCodeBlockBytes,
-                             &sm->full[s]);
-                    bulk_g2s(st + kTokBoxes * kTokBox + kCodeBlockBytes,
-                             a.w_scales + kHeaderBytes + blk * kScaleBlockBytes, kScaleBlockBytes,
-                             &sm->full[s]);
-                    const int x0 = kc * kChunkK;
-                    if (KIND == MOE_PACK_W13) {
-                        tma_load_2d(st, &tok_hi, x0, t.p0, &sm->full[s]);
-                        tma_load_2d(st + kTokBox, &tok_hi, x0 + 64, t.p0, &sm->full[s]);
-                    } else if (kCat) {  // [hi | lo] for K 0-63, then for K 64-127
-                        tma_load_2d(st, &tok_hi, x0, t.p0, &sm->full[s]);
-                        tma_load_2d(st + kTokBox, &tok_lo, x0, t.p0, &sm->full[s]);
-                        tma_load_2d(st + 2 * kTokBox, &tok_hi, x0 + 64, t.p0, &sm->full[s]);
-                        tma_load_2d(st + 3 * kTokBox, &tok_lo, x0 + 64, t.p0, &sm->full[s]);
-                    } else {            // [hi K0-63 | hi K64-127 | lo K0-63 | lo K64-127]
-                        tma_load_2d(st, &tok_hi, x0, t.p0, &sm->full[s]);
-                        tma_load_2d(st + kTokBox, &tok_hi, x0 + 64, t.p0, &sm->full[s]);
-                        tma_load_2d(st + 2 * kTokBox, &tok_lo, x0, t.p0, &sm->full[s]);
-                        tma_load_2d(st + 3 * kTokBox, &tok_lo, x0 + 64, t.p0, &sm->full[s]);
-                    }
-                }
-                __syncwarp();
+        // Walk this producer's own chunks c = pw, pw + NPROD, ... keeping the
+        // tile, K chunk, stage and stage phase incrementally: under the
+        // dequantisation warps' load every instruction of this loop is slow
+        // to issue, so it carries no per-chunk division or tile search.
+        int c = pw, kc = 0, s = pw, p0 = 0;
+        uint32_t phase = 0;
+        int64_t tile = 0, blk0 = 0;
+        auto locate = [&]() {
+            const Tile t = decode_tile<NT>(a, sm, (int)tile);
+            blk0 = ((int64_t)t.e * R + t.rt) * KC;
+            p0 = t.p0;
+        };
+        if (c < my_chunks) {
+            tile = (u_begin + c) / KC;
+            kc = (int)((u_begin + c) % KC);
+            locate();
+        }
+        for (; c < my_chunks; c += NPROD) {
+            if (!warp_wait_bar(&sm->consumed[s], phase ^ 1, sm, a.ctrl, 1)) break;
+            if (elect_one()) {
+                // two copies per chunk: the weight block (codes and scales,
+                // contiguous) and the chunk's token rows
+                uint8_t *st = base + s * kStageBytes;
+                mbar_arrive_expect_tx(&sm->full[s], kStageBytes);
+                bulk_g2s(st + kTokBoxes * kTokBox, a.w + kHeaderBytes + (blk0 + kc) * kBlockBytes,
+                         kBlockBytes, &sm->full[s]);
+                if (KIND == MOE_PACK_W13)
+                    tma_load_3d(st, &tok, 0, p0, 2 * kc, &sm->full[s]);
+                else if (kCat)  // [hi | lo] for K 0-63, then for K 64-127
+                    tma_load_4d(st, &tok, 0, p0, 0, 2 * kc, &sm->full[s]);
+                else            // [hi K0-63 | hi K64-127 | lo K0-63 | lo K64-127]
+                    tma_load_4d(st, &tok, 0, p0, 2 * kc, 0, &sm->full[s]);
             }
-            if (!ok) break;
-            u += k1 - k0;
+            __syncwarp();
+            s += NPROD;
+            if (s >= STAGES) {
+                s -= STAGES;
+                phase ^= 1;
+            }
+            kc += NPROD;
+            if (kc >= KC) {
+                do {
+                    kc -= KC;
+                    ++tile;
+                } while (kc >= KC);
+                if (c + NPROD < my_chunks) locate();
+            }
         }
         // Before the CTA exits, every copy issued must have landed; after an
         // abort elsewhere some were never consumed.  The last copy into each
-        // stage is the only one that can be pending.
-        const int issued = c;
-        for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j)
-            wait_bar_final(&sm->full[j % STAGES], (j / STAGES) & 1);
+        // stage is the only one that can be pending.  Chunks below c with
+        // c % NPROD == pw are this producer's.
+        for (int j = (c > STAGES ? c - STAGES : 0); j < c; ++j)
+            if (j % NPROD == pw) wait_bar_final(&sm->full[j % STAGES], (j / STAGES) & 1);
         __syncwarp();
-    } else if (warp == kMmaWarp) {
-        // ---------------- MMA issuer (converged warp, one elected lane
-        // issues; the same lane every time, so its commits track its MMAs)
-        int c = 0, seg = 0;
+    } else if (warp >= kMmaWarp) {
+        // ---------------- MMA issuers (converged warps, one elected lane
+        // issues; the same lane every time, so its commits track its MMAs).
+        // With two issuers, warp mw takes the chunks c with c % 2 == mw and
+        // accumulates into its own accumulator; the epilogue adds the two.
+        // A single issuer is limited by the issue rate of tcgen05.mma at
+        // small N, not by the tensor pipe, so two of them go about twice
+        // as fast there.
+        const int mw = warp - kMmaWarp;
+        // stage, A buffer and A-buffer phase of this warp's next chunk, kept
+        // incrementally (STAGES and kAB are multiples of MMAW)
+        int s = mw, b = mw;
+        uint32_t bph = 0;
+        const uint64_t desc_base = sdesc_k_sw128(smem_u32(base));
+        int c = 0, seg = 0;  // c: CTA-local index of the segment's first chunk
         bool ok = true;
         for (int64_t u = u_begin; u < u_end && ok; ++seg) {
             const int tile = (int)(u / KC), k0 = (int)(u % KC);
@@ -313,41 +336,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int acc = seg & 1;
             if (!warp_wait_bar(&sm->acc_empty[acc], ((seg >> 1) & 1) ^ 1, sm, a.ctrl, 2)) break;
             tc_fence_after();
-            const uint32_t d_tmem = tb + kAccBase + acc * kAccCols;
-            for (int kc = k0; kc < k1; ++kc, ++c) {
-                const int s = c % STAGES, b = c % kAB;
-                if (!warp_wait_bar(&sm->a_full[b], (c / kAB) & 1, sm, a.ctrl, 3)) {
+            const uint32_t d_tmem = tb + kAccBase + (acc * MMAW + mw) * kAccCols;
+            const int c_end = c + (k1 - k0);
+            bool first = true;
+            for (int cc = c + ((mw - c % MMAW) + MMAW) % MMAW; cc < c_end; cc += MMAW) {
+                if (!warp_wait_bar(&sm->a_full[b], bph, sm, a.ctrl, 3)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // descriptor of the stage's first K slice; a byte offset of
-                // the start address adds offset >> 4 to the descriptor
-                const uint64_t desc0 = sdesc_k_sw128(smem_u32(base + s * kStageBytes));
-                const uint32_t a_tmem = tb + b * kACols;
                 if (elect_one()) {
+                    // 8 MMAs (K = 16 each) over the chunk's A buffer and
+                    // stage; a byte offset of the B start address adds
+                    // offset >> 4 to the descriptor.  One commit then frees
+                    // both.
+                    const uint64_t desc0 = desc_base + (uint64_t)((s * kStageBytes) >> 4);
+                    const uint32_t a_tmem = tb + b * kACols;
 #pragma unroll
                     for (int j = 0; j < kChunkK / 16; ++j) {
-                        const uint32_t acc_flag = (kc > k0 || j > 0) ? 1u : 0u;
+                        const uint32_t acc_flag = (!first || j > 0) ? 1u : 0u;
                         if (kCat) {
                             const uint32_t boff = (j >> 2) * 2 * kTokBox + (j & 3) * 32;
-                            mma_f16_ts(d_tmem, a_tmem + j * 8, desc0 + (boff >> 4), idesc, acc_flag);
+                            mma_f16_ts(d_tmem, a_tmem + j * 8, desc0 + (boff >> 4), idesc,
+                                       acc_flag);
                         } else {
                             const uint32_t boff = (j >> 2) * kTokBox + (j & 3) * 32;
-                            mma_f16_ts(d_tmem, a_tmem + j * 8, desc0 + (boff >> 4), idesc, acc_flag);
+                            mma_f16_ts(d_tmem, a_tmem + j * 8, desc0 + (boff >> 4), idesc,
+                                       acc_flag);
                             if (KIND == MOE_PACK_W2)
                                 mma_f16_ts(d_tmem, a_tmem + j * 8,
                                            desc0 + ((2 * kTokBox + boff) >> 4), idesc, 1u);
                         }
                     }
-                    // one commit frees both the stage and its A buffer
                     tc_commit(&sm->consumed[s]);
                 }
                 __syncwarp();
+                first = false;
+                s += MMAW;
+                if (s >= STAGES) s -= STAGES;
+                b += MMAW;
+                if (b >= kAB) {
+                    b -= kAB;
+                    bph ^= 1;
+                }
             }
             if (!ok) break;
+            // an issuer with no chunk in this segment still arrives (its
+            // accumulator is then not read)
             if (elect_one()) tc_commit(&sm->acc_full[acc]);
             __syncwarp();
+            c = c_end;
             u += k1 - k0;
         }
         // Every MMA issued has completed once `done` fires.
@@ -361,13 +399,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int grp = (warp - kEpiWarps) / 4;
         const int r = (warp & 3) * 32 + lane;  // weight row of the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        // stage, its phase and the A buffer of this group's next chunk, kept
+        // incrementally (STAGES and kAB are multiples of kDqGroups)
+        int s = grp, b = grp;
+        uint32_t ph = 0;
         for (int c = grp; c < my_chunks; c += kDqGroups) {
-            const int s = c % STAGES, b = c % kAB;
-            if (!warp_wait_bar(&sm->full[s], (c / STAGES) & 1, sm, a.ctrl, 4)) break;
-            // A buffer b was last read by the MMAs of chunk c - kAB
+            if (!warp_wait_bar(&sm->full[s], ph, sm, a.ctrl, 4)) break;
+            // A buffer b was last read by the MMAs of chunk c - kAB, whose
+            // stage is kAB stages back
             if (c >= kAB) {
-                const int cp = c - kAB;
-                if (!warp_wait_bar(&sm->consumed[cp % STAGES], (cp / STAGES) & 1, sm, a.ctrl, 5)) break;
+                const int sp = s >= kAB ? s - kAB : s - kAB + STAGES;
+                const uint32_t pp = s >= kAB ? ph : ph ^ 1;
+                if (!warp_wait_bar(&sm->consumed[sp], pp, sm, a.ctrl, 5)) break;
             }
             tc_fence_after();
             const uint8_t *st = base + s * kStageBytes + kTokBoxes * kTokBox;
@@ -401,6 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_wait_st();
             tc_fence_before();
             mbar_arrive(&sm->a_full[b]);
+            s += kDqGroups;
+            if (s >= STAGES) {
+                s -= STAGES;
+                ph ^= 1;
+            }
+            b += kDqGroups;
+            if (b >= kAB) b -= kAB;
         }
     } else {
         // ---------------- epilogue warpgroup (warps 0-3)
@@ -415,23 +465,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int acc = seg & 1;
             if (!warp_wait_bar(&sm->acc_full[acc], (seg >> 1) & 1, sm, a.ctrl, 6)) break;
             tc_fence_after();
-            const uint32_t acc_addr = tb + lane_off + kAccBase + acc * kAccCols;
+            const uint32_t acc_addr = tb + lane_off + kAccBase + acc * MMAW * kAccCols;
+            // with two issuers, the second one had a chunk here unless the
+            // segment is a single chunk that fell to the first (and vice versa)
+            const int c_seg = (int)(u - u_begin);
+            bool has[2] = {true, true};
+            if (MMAW == 2 && k1 - k0 == 1) {
+                has[0] = (c_seg % 2 == 0);
+                has[1] = !has[0];
+            }
             const bool whole = (k0 == 0 && k1 == KC);
             const int which = (u == u_begin) ? 0 : 1;  // first or last segment of this CTA
             float *slot = part + ((size_t)g * 2 + which) * (size_t)NT * kTileRows;
 #pragma unroll 1
             for (int c0 = 0; c0 < t.rows; c0 += 16) {
+                // Sum of the issuers' accumulators (and, with stacked hi/lo
+                // rows, of both halves), always in the same order.
                 uint32_t v[16];
-                tmem_ld16(acc_addr + c0, v);
-                if (kCat) {  // add the lo half, NT columns further on
-                    uint32_t lo[16];
-                    tmem_ld16(acc_addr + NT + c0, lo);
-                    tc_wait_ld();
+                bool any = false;
+#pragma unroll
+                for (int w = 0; w < MMAW; ++w) {
+                    if (!has[w]) continue;
+                    uint32_t x[16];
+                    tmem_ld16(acc_addr + w * kAccCols + c0, x);
+                    if (kCat) {  // add the lo half, NT columns further on
+                        uint32_t lo[16];
+                        tmem_ld16(acc_addr + w * kAccCols + NT + c0, lo);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            x[j] = __float_as_uint(__uint_as_float(x[j]) + __uint_as_float(lo[j]));
+                    } else {
+                        tc_wait_ld();
+                    }
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(lo[j]));
-                } else {
-                    tc_wait_ld();
+                        v[j] = any ? __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(x[j])) : x[j];
+                    any = true;
                 }
                 if (whole) {
                     {
@@ -530,12 +600,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-using KernelFn = void (*)(const TcArgs, const CUtensorMap, const CUtensorMap);
+using KernelFn = void (*)(const TcArgs, const CUtensorMap);
 
 template <int KIND, int NT>
 struct Config {
     static constexpr int kTokBoxes = (KIND == MOE_PACK_W2) ? 4 : 2;
-    static constexpr int kStage = kTokBoxes * NT * 128 + kCodeBlockBytes + kScaleBlockBytes;
+    static constexpr int kStage = kTokBoxes * NT * 128 + kBlockBytes;
     static constexpr int kBudget = 210 * 1024;
     // An even stage count keeps every shared-memory stage with one dequant
     // warpgroup (chunk c and chunk c + kStages have the same parity), so a
@@ -543,7 +613,25 @@ struct Config {
     // and the parity test of the mbarrier cannot alias an older phase.
     static constexpr int kFit = (kBudget / kStage) < kMaxStages ? (kBudget / kStage) : kMaxStages;
     static constexpr int kStages = kFit & ~1;
-    static_assert(kStages >= 2 && kStages % kDqGroups == 0, "stage count must be a multiple of the dequant groups");
+    // Warp roles.  Each mbarrier wait costs a shared-memory round trip of
+    // over a hundred cycles even when the phase is complete, and every
+    // instruction of the small control loops waits behind the dequantisation
+    // warps' arithmetic, so the control roles are split over several warps
+    // whose waits overlap:
+    //  * four dequantisation warpgroups (each stage stays with one of them,
+    //    which needs a stage count divisible by four), else two;
+    //  * two TMA producers (each owns every other stage);
+    //  * two MMA issuers where N is small enough for the issue rate of
+    //    tcgen05.mma, not the tensor pipe, to limit, and their
+    //    accumulators fit next to the A buffers in tensor memory.
+    static constexpr int kDq = (kStages % 4 == 0) ? 4 : 2;
+    static constexpr int kAB = kStages >= 4 ? 4 : 2;
+    static constexpr int kAccCols = (KIND == MOE_PACK_W2 && NT <= 64) ? 2 * NT : NT;
+    static constexpr int kMma = (kAccCols <= 64 && kAB * kACols + 4 * kAccCols <= (int)kTmemCols)
+                                    ? 2 : 1;
+    static constexpr int kProd = 2;
+    static constexpr int kThreads = threads_for(kDq, kProd, kMma);
+    static_assert(kStages >= 2 && kStages % kDq == 0, "stage count must be a multiple of the dequant groups");
     // The kernel is persistent with one CTA per SM and allocates all of
     // tensor memory: asking for more than half of an SM's shared memory
     // keeps the scheduler from ever placing two of its CTAs on one SM (the
@@ -551,16 +639,24 @@ struct Config {
     static constexpr size_t kMinSmem = 120 * 1024;
     static constexpr size_t kNeed = (size_t)kStages * kStage + sizeof(Smem) + 1024;
     static constexpr size_t kSmem = kNeed > kMinSmem ? kNeed : kMinSmem;
-    static KernelFn fn() { return gemm_tc_kernel<KIND, NT, kStages>; }
+    static KernelFn fn() { return gemm_tc_kernel<KIND, NT, kStages, kDq, kProd, kMma>; }
 };
 
+template <int KIND, int NT>
+bool pick_nt(KernelFn *fn, size_t *smem, int *threads) {
+    *fn = Config<KIND, NT>::fn();
+    *smem = Config<KIND, NT>::kSmem;
+    *threads = Config<KIND, NT>::kThreads;
+    return true;
+}
+
 template <int KIND>
-bool pick(int nt, KernelFn *fn, size_t *smem) {
+bool pick(int nt, KernelFn *fn, size_t *smem, int *threads) {
     switch (nt) {
-        case 16: *fn = Config<KIND, 16>::fn(); *smem = Config<KIND, 16>::kSmem; return true;
-        case 32: *fn = Config<KIND, 32>::fn(); *smem = Config<KIND, 32>::kSmem; return true;
-        case 64: *fn = Config<KIND, 64>::fn(); *smem = Config<KIND, 64>::kSmem; return true;
-        case 128: *fn = Config<KIND, 128>::fn(); *smem = Config<KIND, 128>::kSmem; return true;
+        case 16: return pick_nt<KIND, 16>(fn, smem, threads);
+        case 32: return pick_nt<KIND, 32>(fn, smem, threads);
+        case 64: return pick_nt<KIND, 64>(fn, smem, threads);
+        case 128: return pick_nt<KIND, 128>(fn, smem, threads);
     }
     return false;
 }
@@ -592,11 +688,30 @@ EncodeTiledFn encoder() {
 bool make_token_map(CUtensorMap *map, const void *ptr, int rows, int cols, int box_rows) {
     EncodeTiledFn enc = encoder();
     if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-    cuuint32_t es[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+    cuuint64_t dims[3] = {64, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)cols / 64};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 2};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+bool make_act_map(CUtensorMap *map, const void *hi, const void *lo, int rows, int cols,
+                  int box_rows, bool stacked) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return false;
+    const uintptr_t h = reinterpret_cast<uintptr_t>(hi), l = reinterpret_cast<uintptr_t>(lo);
+    if (l <= h || (l - h) % 16) return false;
+    const cuuint64_t r = (cuuint64_t)(rows > 0 ? rows : 1), kh = (cuuint64_t)cols / 64;
+    const cuuint64_t row_b = (cuuint64_t)cols * 2, half_b = l - h;
+    // dimension 0: 64 columns; 1: rows; then (hi/lo, K half) or (K half, hi/lo)
+    cuuint64_t dims[4] = {64, r, stacked ? 2 : kh, stacked ? kh : 2};
+    cuuint64_t strides[3] = {row_b, stacked ? half_b : 128, stacked ? 128 : half_b};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 2, 2};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void *>(hi), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
@@ -616,18 +731,19 @@ int tc_grid(int device) {
     return sms[device];
 }
 
-cudaError_t launch_gemm_tc(const TcArgs &args, const CUtensorMap &hi, const CUtensorMap &lo,
-                           int grid, cudaStream_t s, bool pdl) {
+cudaError_t launch_gemm_tc(const TcArgs &args, const CUtensorMap &tok, int grid, cudaStream_t s,
+                           bool pdl) {
     KernelFn fn = nullptr;
     size_t smem = 0;
-    const bool ok = (args.kind == MOE_PACK_W13) ? pick<MOE_PACK_W13>(args.nt, &fn, &smem)
-                                                : pick<MOE_PACK_W2>(args.nt, &fn, &smem);
+    int threads = 0;
+    const bool ok = (args.kind == MOE_PACK_W13) ? pick<MOE_PACK_W13>(args.nt, &fn, &smem, &threads)
+                                                : pick<MOE_PACK_W2>(args.nt, &fn, &smem, &threads);
     if (!ok) return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -635,7 +751,7 @@ cudaError_t launch_gemm_tc(const TcArgs &args, const CUtensorMap &hi, const CUte
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, fn, args, hi, lo);
+    return cudaLaunchKernelEx(&cfg, fn, args, tok);
 }
 
 }  // namespace moe

@@ -10,8 +10,7 @@ namespace moe {
 constexpr int kMaxStages = 16;
 
 struct TcArgs {
-    const uint8_t *w_codes;      // prepacked codes (header included)
-    const uint8_t *w_scales;     // prepacked scales (header included)
+    const uint8_t *w;            // prepacked weights (header included)
     const int32_t *offsets;      // [E+1] sorted-row offsets per expert
     const int32_t *tile_prefix;  // [E+1] token-tile prefix per expert (tile width nt)
     int32_t *tickets;            // per (expert tile x weight tile); zeroed by align
@@ -24,11 +23,23 @@ struct TcArgs {
     Ctrl *ctrl;
 };
 
-// 2-D fp16 tensor map over [rows][cols] (row-major), box {64, box_rows},
-// 128-byte swizzle, zero fill out of bounds.
+// Whether the down GEMM stacks the hi and lo rows of its activation into one
+// B operand (small token tiles); the kernel and its tensor map agree on it.
+inline bool stacked_hi_lo(int nt) { return nt <= 64; }
+
+// Token operand of the gate+up GEMM: fp16 [rows][cols] (row-major) seen as
+// 3-D (64 columns, rows, cols/64) so that one copy brings a 128-column K
+// chunk of box_rows rows, stored as two 64-column slabs of box_rows x 128 B
+// (128-byte swizzle, zero fill beyond the last row).
 bool make_token_map(CUtensorMap *map, const void *ptr, int rows, int cols, int box_rows);
+// Token operand of the down GEMM: the hi and lo fp16 halves of the
+// activation (lo at a fixed byte distance after hi) as one 4-D map, so that
+// one copy brings both halves of a K chunk: slabs in the order
+// [K half][hi, lo] when `stacked`, [hi, lo][K half] otherwise.
+bool make_act_map(CUtensorMap *map, const void *hi, const void *lo, int rows, int cols,
+                  int box_rows, bool stacked);
 int tc_grid(int device);
-cudaError_t launch_gemm_tc(const TcArgs &args, const CUtensorMap &hi, const CUtensorMap &lo,
-                           int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_gemm_tc(const TcArgs &args, const CUtensorMap &tok, int grid, cudaStream_t s,
+                           bool pdl);
 
 }  // namespace moe

@@ -13,15 +13,15 @@ namespace moe {
 // ---------------------------------------------------------------------------
 // Prepacked weight layout.
 //
-// Every prepacked buffer starts with a 256-byte header, then blocks.  A block
-// covers one 128-row tile of one expert and one 128-element K chunk:
-//   code block  (8192 B): 4 pieces x 128 rows x 16 B; piece pc of row r at
-//                         byte (pc*128 + r)*16 holds K elements
-//                         [32pc, 32pc+32) of the chunk as 4 words; word w
-//                         covers elements 8w..8w+7 with nibbles, low to high,
-//                         in element order 0,2,4,6,1,3,5,7.
-//   scale block (1024 B): 128 rows x 4 groups of fp16, row r group g at
-//                         byte (r*4 + g)*2.
+// A prepacked buffer starts with a 256-byte header, then blocks of 9216 B.
+// A block covers one 128-row tile of one expert and one 128-element K chunk:
+//   bytes [0, 8192)    codes: 4 pieces x 128 rows x 16 B; piece pc of row r
+//                      at byte (pc*128 + r)*16 holds K elements
+//                      [32pc, 32pc+32) of the chunk as 4 words; word w
+//                      covers elements 8w..8w+7 with nibbles, low to high,
+//                      in element order 0,2,4,6,1,3,5,7.
+//   bytes [8192, 9216) scales: 128 rows x 4 groups of fp16, row r group g
+//                      at byte 8192 + (r*4 + g)*2.
 // Block index = (e * tiles_per_expert + tile) * k_chunks + chunk.
 // For w13, tile t holds gate rows 64t..64t+63 at even tile rows (row 2j =
 // gate row 64t+j) and the matching up rows at odd tile rows (2j+1).
@@ -31,28 +31,25 @@ constexpr int kChunkK = 128;
 constexpr int kGroup = 32;
 constexpr int kCodeBlockBytes = kTileRows * kChunkK / 2;       // 8192
 constexpr int kScaleBlockBytes = kTileRows * (kChunkK / kGroup) * 2;  // 1024
+constexpr int kBlockBytes = kCodeBlockBytes + kScaleBlockBytes;       // 9216
 constexpr int kHeaderBytes = 256;
 
 constexpr uint32_t kPackMagic = 0x5034574Du;  // "MW4P"
-constexpr uint32_t kPackVersion = 1;
-constexpr uint32_t kPartCodes = 1, kPartScales = 2;
+constexpr uint32_t kPackVersion = 2;  // 2: codes and scales in one block
 
 struct PackHeader {
     uint32_t magic;
     uint32_t version;
     uint32_t kind;    // MOE_PACK_W13 / MOE_PACK_W2
-    uint32_t part;    // kPartCodes / kPartScales
+    uint32_t block_bytes;  // kBlockBytes
     int32_t E, N, K, group;
     int32_t status;   // MOE_OK once the prepack finished and validated
     int32_t pad[3];
 };
 static_assert(sizeof(PackHeader) <= kHeaderBytes, "header too large");
 
-inline size_t code_bytes(int E, int N, int K) {
-    return kHeaderBytes + (size_t)E * (N / kTileRows) * (K / kChunkK) * kCodeBlockBytes;
-}
-inline size_t scale_bytes(int E, int N, int K) {
-    return kHeaderBytes + (size_t)E * (N / kTileRows) * (K / kChunkK) * kScaleBlockBytes;
+inline size_t packed_bytes(int E, int N, int K) {
+    return kHeaderBytes + (size_t)E * (N / kTileRows) * (K / kChunkK) * kBlockBytes;
 }
 
 // ---------------------------------------------------------------------------
@@ -94,7 +91,7 @@ FwdLayout fwd_layout(int M, int k, int E, int H, int I);
 
 // moe_w4a16_forward on a scratch buffer the caller of this function chose.
 moe_status_t forward_on_scratch(const uint16_t *hidden, const int32_t *ids, const float *topk_w,
-                                const void *w13, const void *s13, const void *w2, const void *s2,
+                                const void *w13, const void *w2,
                                 uint16_t *out, int M, int k, int E, int H, int I, void *scratch,
                                 size_t scratch_bytes, moe_stream_t stream);
 
@@ -113,6 +110,7 @@ struct AlignArgs {
 };
 cudaError_t launch_align(const AlignArgs &a, cudaStream_t s);
 
+// Both write into the blocks after the header of a prepacked buffer `dst`.
 cudaError_t launch_prepack_codes(int kind, const uint8_t *q, int E, int N, int K,
                                  uint8_t *dst, cudaStream_t s);
 cudaError_t launch_prepack_scales(int kind, const uint16_t *sc, int E, int N, int K,

@@ -19,9 +19,9 @@ __device__ __forceinline__ int canonical_row(int kind, int N, int tile, int r) {
     return tile * kTileRows + r;
 }
 
-// One thread per output 32-bit word of codes.
+// One thread per output 32-bit word of codes (the first 8 KiB of a block).
 __global__ void prepack_codes_kernel(int kind, const uint32_t *__restrict__ q, int E, int N,
-                                     int K, uint32_t *__restrict__ dst) {
+                                     int K, uint8_t *__restrict__ blocks) {
     const int tiles = N / kTileRows, chunks = K / kChunkK;
     const int64_t words_per_block = kCodeBlockBytes / 4;
     const int64_t total = (int64_t)E * tiles * chunks * words_per_block;
@@ -45,14 +45,15 @@ __global__ void prepack_codes_kernel(int kind, const uint32_t *__restrict__ q, i
             const int slot = (i & 1) ? 4 + (i >> 1) : (i >> 1);
             o |= v << (4 * slot);
         }
-        dst[wd] = o;
+        reinterpret_cast<uint32_t *>(blocks + b * kBlockBytes)[wib] = o;
     }
 }
 
-// One thread per output fp16 scale.  A scale must be zero, NaN, infinite or
-// of magnitude in [2^-14, 8188] so that (q - 8) * scale is exact in fp16.
+// One thread per output fp16 scale (the last 1 KiB of a block).  A scale
+// must be zero, NaN, infinite or of magnitude in [2^-14, 8188] so that
+// (q - 8) * scale is exact in fp16.
 __global__ void prepack_scales_kernel(int kind, const uint16_t *__restrict__ s, int E, int N,
-                                      int K, __half *__restrict__ dst, int32_t *bad_flag) {
+                                      int K, uint8_t *__restrict__ blocks, int32_t *bad_flag) {
     const int tiles = N / kTileRows, chunks = K / kChunkK, groups = K / kGroup;
     const int per_block = kTileRows * (kChunkK / kGroup);
     const int64_t total = (int64_t)E * tiles * chunks * per_block;
@@ -70,7 +71,8 @@ __global__ void prepack_scales_kernel(int kind, const uint16_t *__restrict__ s, 
         const bool ok = (f == 0.0f) || isnan(f) || isinf(f) ||
                         (a >= 6.103515625e-05f && a <= 8188.0f);
         if (!ok) atomicExch(bad_flag, 1);
-        dst[i] = __float2half_rn(f);
+        reinterpret_cast<__half *>(blocks + b * kBlockBytes + kCodeBlockBytes)[within] =
+            __float2half_rn(f);
     }
 }
 
@@ -85,16 +87,15 @@ cudaError_t launch_prepack_codes(int kind, const uint8_t *q, int E, int N, int K
                                  cudaStream_t s) {
     const int64_t words = (int64_t)E * (N / kTileRows) * (K / kChunkK) * (kCodeBlockBytes / 4);
     prepack_codes_kernel<<<grid_for(words), 256, 0, s>>>(
-        kind, reinterpret_cast<const uint32_t *>(q), E, N, K,
-        reinterpret_cast<uint32_t *>(dst + kHeaderBytes));
+        kind, reinterpret_cast<const uint32_t *>(q), E, N, K, dst + kHeaderBytes);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prepack_scales(int kind, const uint16_t *sc, int E, int N, int K, uint8_t *dst,
                                   int32_t *bad_flag, cudaStream_t s) {
     const int64_t n = (int64_t)E * (N / kTileRows) * (K / kChunkK) * (kScaleBlockBytes / 2);
-    prepack_scales_kernel<<<grid_for(n), 256, 0, s>>>(
-        kind, sc, E, N, K, reinterpret_cast<__half *>(dst + kHeaderBytes), bad_flag);
+    prepack_scales_kernel<<<grid_for(n), 256, 0, s>>>(kind, sc, E, N, K, dst + kHeaderBytes,
+                                                      bad_flag);
     return cudaGetLastError();
 }
 

@@ -50,8 +50,7 @@ moe_status_t scratch_address(void **out) {
 
 extern "C" moe_status_t moe_w4a16_forward_static(const uint16_t *hidden, const int32_t *topk_ids,
                                                  const float *topk_w, const void *w13,
-                                                 const void *s13, const void *w2, const void *s2,
-                                                 uint16_t *out, int M, int k, int E, int H, int I,
+                                                 const void *w2, uint16_t *out, int M, int k, int E, int H, int I,
                                                  moe_stream_t stream) {
     const size_t need = moe_w4a16_workspace_size(M, k, E, H, I);
     if (need == 0) return MOE_ERR_INVALID_ARG;
@@ -59,6 +58,6 @@ extern "C" moe_status_t moe_w4a16_forward_static(const uint16_t *hidden, const i
     void *scratch = nullptr;
     const moe_status_t st = moe::scratch_address(&scratch);
     if (st != MOE_OK) return st;
-    return moe::forward_on_scratch(hidden, topk_ids, topk_w, w13, s13, w2, s2, out, M, k, E, H, I,
+    return moe::forward_on_scratch(hidden, topk_ids, topk_w, w13, w2, out, M, k, E, H, I,
                                    scratch, moe::kStaticScratchBytes, stream);
 }

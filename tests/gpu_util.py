@@ -58,7 +58,7 @@ class DeviceLayer:
         wd = to_dev(w)
         M = ids.shape[0]
         ws = workspace if workspace is not None else moe.Workspace(M, L.k, L.E, L.H, L.I, "cuda")
-        out = moe.forward(xd, idd, wd, self.p13[0], self.p13[1], self.p2[0], self.p2[1],
+        out = moe.forward(xd, idd, wd, self.p13, self.p2,
                           L.E, L.I, workspace=ws, stream=stream)
         return out, ws
 

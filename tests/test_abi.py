@@ -45,15 +45,15 @@ def test_status_strings(lib):
     assert "UNKNOWN" in moe.moe_status_string(99)
 
 
-def test_prepack_sizes(lib):
-    st, c, s = moe.moe_w4a16_prepack_sizes(moe.MOE_PACK_W13, 384, 4096, 7168, 32)
+def test_prepack_size(lib):
+    st, b = moe.moe_w4a16_prepack_size(moe.MOE_PACK_W13, 384, 4096, 7168, 32)
     assert st == moe.MOE_OK
-    assert c == 256 + 384 * 4096 * 7168 // 2
-    assert s == 256 + 384 * 4096 * (7168 // 32) * 2
+    # header + int4 codes + one fp16 scale per 32 weights
+    assert b == 256 + 384 * 4096 * 7168 // 2 + 384 * 4096 * (7168 // 32) * 2
     for bad in [(3, 8, 256, 256, 32), (1, 8, 256, 256, 64), (1, 0, 256, 256, 32),
                 (1, 8, 200, 256, 32), (1, 8, 256, 96, 32)]:
-        st, c, s = moe.moe_w4a16_prepack_sizes(*bad)
-        assert st == moe.MOE_ERR_INVALID_ARG and c == 0 and s == 0
+        st, b = moe.moe_w4a16_prepack_size(*bad)
+        assert st == moe.MOE_ERR_INVALID_ARG and b == 0
 
 
 def test_workspace_sizes(lib):
@@ -71,12 +71,12 @@ def test_workspace_sizes(lib):
 
 
 def _fwd(lib, **kw):
-    args = dict(hidden=4096, ids=4096, w=4096, w13=4096, s13=4096, w2=4096, s2=4096, out=4096,
+    args = dict(hidden=4096, ids=4096, w=4096, w13=4096, w2=4096, out=4096,
                 M=4, k=2, E=8, H=256, I=128, ws=4096, ws_bytes=1 << 30)
     args.update(kw)
-    return lib.moe_w4a16_forward(args["hidden"], args["ids"], args["w"], args["w13"], args["s13"],
-                                 args["w2"], args["s2"], args["out"], args["M"], args["k"],
-                                 args["E"], args["H"], args["I"], args["ws"], args["ws_bytes"], None)
+    return lib.moe_w4a16_forward(args["hidden"], args["ids"], args["w"], args["w13"], args["w2"],
+                                 args["out"], args["M"], args["k"], args["E"], args["H"],
+                                 args["I"], args["ws"], args["ws_bytes"], None)
 
 
 def test_forward_host_validation(lib):
@@ -103,11 +103,13 @@ def test_align_and_prepack_host_validation(lib):
     assert lib.moe_align(None, 4, 2, 8, p, p, p, p, p, 1 << 20, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_align(p, 4, 2, 8, p, p, p, p, p + 8, 1 << 20, None) == moe.MOE_ERR_MISALIGNED
     assert lib.moe_align(p, 4, 2, 8, p, p, p, p, p, 16, None) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
-    assert lib.moe_w4a16_prepack(1, p, p, 8, 256, 256, 32, p, 16, p, 1 << 30, None) == \
+    assert lib.moe_w4a16_prepack(1, p, p, 8, 256, 256, 32, p, 16, None) == \
         moe.MOE_ERR_WORKSPACE_TOO_SMALL
-    assert lib.moe_w4a16_prepack(1, p + 4, p, 8, 256, 256, 32, p, 1 << 30, p, 1 << 30, None) == \
+    assert lib.moe_w4a16_prepack(1, p + 4, p, 8, 256, 256, 32, p, 1 << 30, None) == \
         moe.MOE_ERR_MISALIGNED
-    assert lib.moe_w4a16_prepack(1, None, p, 8, 256, 256, 32, p, 1 << 30, p, 1 << 30, None) == \
+    assert lib.moe_w4a16_prepack(1, p, p, 8, 256, 256, 32, p + 16, 1 << 30, None) == \
+        moe.MOE_ERR_MISALIGNED
+    assert lib.moe_w4a16_prepack(1, None, p, 8, 256, 256, 32, p, 1 << 30, None) == \
         moe.MOE_ERR_INVALID_ARG
 
 

@@ -34,7 +34,7 @@ def test_swapped_buffers_report_bad_layout(toy_layer):
     ids, w = synth.routing(4, L)
     ws = moe.Workspace(4, L.k, L.E, L.H, L.I, "cuda")
     p13, p2 = toy_layer.p13, toy_layer.p2
-    moe.forward(x, gu.to_dev(ids), gu.to_dev(w), p2[0], p2[1], p13[0], p13[1], L.E, L.I,
+    moe.forward(x, gu.to_dev(ids), gu.to_dev(w), p2, p13, L.E, L.I,
                 workspace=ws)
     assert moe.moe_w4a16_get_device_status(ws.buf)[0] == moe.MOE_ERR_BAD_LAYOUT
 
@@ -69,6 +69,6 @@ def test_m_zero_is_a_noop(toy_layer):
     x = torch.zeros((0, L.H), dtype=torch.bfloat16, device="cuda")
     ids = torch.zeros((0, L.k), dtype=torch.int32, device="cuda")
     w = torch.zeros((0, L.k), dtype=torch.float32, device="cuda")
-    moe.forward(x, ids, w, toy_layer.p13[0], toy_layer.p13[1], toy_layer.p2[0], toy_layer.p2[1],
+    moe.forward(x, ids, w, toy_layer.p13, toy_layer.p2,
                 L.E, L.I, out=out, workspace=ws)
     torch.cuda.synchronize()

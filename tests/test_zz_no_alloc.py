@@ -32,7 +32,7 @@ def _static_matches_regular(dl, wl, M):
     idd, wd = gu.to_dev(ids), gu.to_dev(w)
     for _ in range(2):
         out = torch.full((M, L.H), float("nan"), dtype=torch.bfloat16, device="cuda")
-        st = moe.moe_w4a16_forward_static(xd, idd, wd, dl.p13[0], dl.p13[1], dl.p2[0], dl.p2[1],
+        st = moe.moe_w4a16_forward_static(xd, idd, wd, dl.p13, dl.p2,
                                           out, M, L.k, L.E, L.H, L.I)
         assert st == moe.MOE_OK, moe.moe_status_string(st)
         torch.cuda.synchronize()
@@ -63,6 +63,6 @@ def test_static_rejects_sizes_beyond_the_array(e384_layer):
     w = torch.zeros((M, L.k), dtype=torch.float32, device="cuda")
     out = torch.zeros((M, L.H), dtype=torch.bfloat16, device="cuda")
     dl = e384_layer
-    st = moe.moe_w4a16_forward_static(x, ids, w, dl.p13[0], dl.p13[1], dl.p2[0], dl.p2[1], out,
+    st = moe.moe_w4a16_forward_static(x, ids, w, dl.p13, dl.p2, out,
                                       M, L.k, L.E, L.H, L.I)
     assert st == moe.MOE_ERR_WORKSPACE_TOO_SMALL
