@@ -159,9 +159,10 @@ moe_status_t moe_w4a16_prepack(int kind, const uint8_t *q_canon, const uint16_t 
     // a scale outside the exact range sets the header's status, which makes
     // every later forward reject the buffer
     int32_t *flag = &reinterpret_cast<PackHeader *>(d)->status;
+    int32_t *wide = &reinterpret_cast<PackHeader *>(d)->wide_scales;
     if (cudaMemcpyAsync(d, &h, sizeof h, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         launch_prepack_codes(kind, q_canon, E, N, K, d, s) != cudaSuccess ||
-        launch_prepack_scales(kind, scales, E, N, K, d, flag, s) != cudaSuccess ||
+        launch_prepack_scales(kind, scales, E, N, K, d, flag, wide, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;

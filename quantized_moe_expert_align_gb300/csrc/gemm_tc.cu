@@ -36,6 +36,7 @@
 // MOE_ERR_DEVICE_TIMEOUT and the CTA winds down without hanging.
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "device_common.cuh"
 #include "sm100.cuh"
@@ -56,6 +57,7 @@ constexpr int kMaxABufs = 4;                  // TMEM A buffers (64 columns each
 constexpr int kACols = kChunkK / 2;           // 64 fp16 pairs per row per chunk
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitCycles = 1ll << 31;  // bounded waits give up after ~1-2 s
+constexpr uint32_t kSleepNs = 20000;          // longest sleep of one poll of a wait
 
 struct Smem {
     uint64_t full[kMaxStages];      // stage loaded (TMA transaction bytes)
@@ -66,6 +68,7 @@ struct Smem {
     uint32_t tmem_base;
     int abort;
     int bad;
+    int wide;  // the weights have scales beyond the fused dequantisation's range
     // per-expert token-tile prefix and sorted-row offsets, copied once so
     // that decoding a tile is a search in shared, not global, memory
     int32_t tile_prefix[1025];
@@ -79,15 +82,13 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Smem *s
                                          int who) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0) {
-            if (*(volatile int *)&sm->abort) return false;
-            if (clock64() - t0 > kWaitCycles) {
-                atomicExch(&sm->abort, 1);
-                set_status(ctrl, MOE_ERR_DEVICE_TIMEOUT, who);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
+        if (*(volatile int *)&sm->abort) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            atomicExch(&sm->abort, 1);
+            set_status(ctrl, MOE_ERR_DEVICE_TIMEOUT, who);
+            return false;
         }
     }
 }
@@ -150,31 +151,52 @@ __device__ __forceinline__ Tile decode_tile(const TcArgs &a, const Smem *sm, int
     return t;
 }
 
-// (q - 8) * scale for the 8 codes of one word, as 4 fp16 pairs in element
-// order.  Nibbles are stored in element order 0,2,4,6,1,3,5,7, so masking
-// 0x000F000F yields elements (0,1), masking 0x00F000F0 yields 16x elements
-// (2,3), and the same after a shift by 8 gives (4,5) and (6,7).  OR-ing the
-// exponent of 1024 makes 1024 + q (or 1024 + 16q) exactly; subtracting 1032
-// (or scaling by 1/16 and adding -72) gives q - 8 exactly, and the product
-// with an fp16 scale of magnitude >= 2^-14 is exact (at most 11 bits).
-__device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, uint32_t (&o)[4]) {
+// Dequantisation of one 32-bit code word: the 8 weights (q - 8) * scale,
+// exactly, as 4 fp16 pairs in element order (elements 2j, 2j+1 -> o[j]).
+// Element i's code sits at bit nibble_pos(i) = 6, 22, 10, 26, 14, 30, 18, 2
+// (the one at 30 wraps to bits 0-1), so that
+//  * w & 0x03C003C0 holds elements 0 and 1 at bits 6-9 of each half, and a
+//    rotation by 4 brings elements 2 and 3 there: OR-ing the exponent of 16
+//    makes the fp16 values 16 + q, and one fused multiply-add with the
+//    scale s and -24 s gives (16 + q) s - 24 s = (q - 8) s, rounded once
+//    from the exact value, which is itself an fp16 number (s has at most 8
+//    significant bits, q - 8 at most 4);
+//  * a rotation by 14 brings elements 4, 5 to bits 0-3 and 6, 7 to bits
+//    4-7 of each half: OR-ing the exponent of 1024 makes 1024 + q (or
+//    1024 + 16 q), minus 1032 (or times 1/16 minus 72) is q - 8 exactly,
+//    then a product with s.
+// The fused form needs -24 s in fp16 (|s| <= 65504/24); buffers with wider
+// or infinite scales use exact_pairs for elements 0-3 as well.  The two
+// ways split the work evenly between the integer and the fp16 pipes.
+__device__ __forceinline__ uint32_t rotr(uint32_t x, int n) { return __funnelshift_r(x, x, n); }
+
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+
+// (1024 + q) and (1024 + 16 q) at bits 0-3 / 4-7 of each half of x -> 2 pairs
+__device__ __forceinline__ void exact_pairs(uint32_t x, __half2 s2, uint32_t &lo, uint32_t &hi) {
     const uint32_t magic = 0x64006400u;
-    const __half2 bias_lo = __floats2half2_rn(1032.f, 1032.f);
-    const __half2 sixteenth = __floats2half2_rn(0.0625f, 0.0625f);
-    const __half2 bias_hi = __floats2half2_rn(-72.f, -72.f);
-    const uint32_t w8 = w >> 8;
-    uint32_t r0 = (w & 0x000F000Fu) | magic;
-    uint32_t r1 = (w & 0x00F000F0u) | magic;
-    uint32_t r2 = (w8 & 0x000F000Fu) | magic;
-    uint32_t r3 = (w8 & 0x00F000F0u) | magic;
-    __half2 h0 = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&r0), bias_lo), s2);
-    __half2 h1 = __hmul2(__hfma2(*reinterpret_cast<__half2 *>(&r1), sixteenth, bias_hi), s2);
-    __half2 h2 = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&r2), bias_lo), s2);
-    __half2 h3 = __hmul2(__hfma2(*reinterpret_cast<__half2 *>(&r3), sixteenth, bias_hi), s2);
-    o[0] = *reinterpret_cast<uint32_t *>(&h0);
-    o[1] = *reinterpret_cast<uint32_t *>(&h1);
-    o[2] = *reinterpret_cast<uint32_t *>(&h2);
-    o[3] = *reinterpret_cast<uint32_t *>(&h3);
+    uint32_t r0 = (x & 0x000F000Fu) | magic;
+    uint32_t r1 = (x & 0x00F000F0u) | magic;
+    lo = h2u(__hmul2(__hsub2(*reinterpret_cast<__half2 *>(&r0), __floats2half2_rn(1032.f, 1032.f)),
+                     s2));
+    hi = h2u(__hmul2(__hfma2(*reinterpret_cast<__half2 *>(&r1), __floats2half2_rn(0.0625f, 0.0625f),
+                             __floats2half2_rn(-72.f, -72.f)),
+                     s2));
+}
+
+// s2 = (s, s); c2 = (-24 s, -24 s) when FUSED
+template <bool FUSED>
+__device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, __half2 c2, uint32_t (&o)[4]) {
+    if (FUSED) {
+        const uint32_t magic16 = 0x4C004C00u, mask = 0x03C003C0u;
+        uint32_t r0 = (w & mask) | magic16;
+        uint32_t r1 = (rotr(w, 4) & mask) | magic16;
+        o[0] = h2u(__hfma2(*reinterpret_cast<__half2 *>(&r0), s2, c2));
+        o[1] = h2u(__hfma2(*reinterpret_cast<__half2 *>(&r1), s2, c2));
+    } else {
+        exact_pairs(rotr(w, 6), s2, o[0], o[1]);
+    }
+    exact_pairs(rotr(w, 14), s2, o[2], o[3]);
 }
 
 template <int KIND, int NT, int STAGES, int DQG, int NPROD, int MMAW>
@@ -228,6 +250,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
         mbar_init(&sm->done, MMAW);
         sm->abort = 0;
         sm->bad = !header_ok(a.w, KIND, a.E, a.N, a.K);
+        sm->wide = reinterpret_cast<const PackHeader *>(a.w)->wide_scales != 0;
         if (sm->bad && g == 0) set_status(a.ctrl, MOE_ERR_BAD_LAYOUT, KIND);
         fence_barrier_init();
     }
@@ -397,6 +420,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     } else if (warp >= kEpiWarps) {
         // ---------------- dequantisation warpgroups
         const int grp = (warp - kEpiWarps) / 4;
+        const bool wide = sm->wide != 0;
         const int r = (warp & 3) * 32 + lane;  // weight row of the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         // stage, its phase and the A buffer of this group's next chunk, kept
@@ -420,27 +444,37 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                          : "=r"(sc.x), "=r"(sc.y) : "r"(st_s + kCodeBlockBytes + r * 8));
             const uint32_t scw[2] = {sc.x, sc.y};
             const uint32_t a_addr = tb + lane_off + b * kACols;
+            // one 32-element scale group per piece: load, dequantise, store
+            // the piece's 16 columns of the A buffer
+            auto pieces = [&](auto fused) {
+                constexpr bool kFused = decltype(fused)::value;
 #pragma unroll
-            for (int pc = 0; pc < 4; ++pc) {
-                uint4 q;
-                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w)
-                             : "r"(st_s + (pc * kTileRows + r) * 16));
-                const uint32_t sbits = (scw[pc >> 1] >> ((pc & 1) * 16)) & 0xFFFFu;
-                const __half hs = __ushort_as_half((unsigned short)sbits);
-                const __half2 s2 = __halves2half2(hs, hs);
-                uint32_t v[16];
-                uint32_t o[4];
-                dequant_word(q.x, s2, o);
-                v[0] = o[0]; v[1] = o[1]; v[2] = o[2]; v[3] = o[3];
-                dequant_word(q.y, s2, o);
-                v[4] = o[0]; v[5] = o[1]; v[6] = o[2]; v[7] = o[3];
-                dequant_word(q.z, s2, o);
-                v[8] = o[0]; v[9] = o[1]; v[10] = o[2]; v[11] = o[3];
-                dequant_word(q.w, s2, o);
-                v[12] = o[0]; v[13] = o[1]; v[14] = o[2]; v[15] = o[3];
-                tmem_st16(a_addr + pc * 16, v);
-            }
+                for (int pc = 0; pc < 4; ++pc) {
+                    uint4 q;
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w)
+                                 : "r"(st_s + (pc * kTileRows + r) * 16));
+                    const uint32_t sbits = (scw[pc >> 1] >> ((pc & 1) * 16)) & 0xFFFFu;
+                    const __half hs = __ushort_as_half((unsigned short)sbits);
+                    const __half2 s2 = __halves2half2(hs, hs);
+                    const __half2 c2 = kFused ? __hmul2(s2, __floats2half2_rn(-24.f, -24.f)) : s2;
+                    uint32_t v[16];
+                    uint32_t o[4];
+                    dequant_word<kFused>(q.x, s2, c2, o);
+                    v[0] = o[0]; v[1] = o[1]; v[2] = o[2]; v[3] = o[3];
+                    dequant_word<kFused>(q.y, s2, c2, o);
+                    v[4] = o[0]; v[5] = o[1]; v[6] = o[2]; v[7] = o[3];
+                    dequant_word<kFused>(q.z, s2, c2, o);
+                    v[8] = o[0]; v[9] = o[1]; v[10] = o[2]; v[11] = o[3];
+                    dequant_word<kFused>(q.w, s2, c2, o);
+                    v[12] = o[0]; v[13] = o[1]; v[14] = o[2]; v[15] = o[3];
+                    tmem_st16(a_addr + pc * 16, v);
+                }
+            };
+            if (wide)
+                pieces(std::false_type{});
+            else
+                pieces(std::true_type{});
             tc_wait_st();
             tc_fence_before();
             mbar_arrive(&sm->a_full[b]);

@@ -18,8 +18,9 @@ namespace moe {
 //   bytes [0, 8192)    codes: 4 pieces x 128 rows x 16 B; piece pc of row r
 //                      at byte (pc*128 + r)*16 holds K elements
 //                      [32pc, 32pc+32) of the chunk as 4 words; word w
-//                      covers elements 8w..8w+7 with nibbles, low to high,
-//                      in element order 0,2,4,6,1,3,5,7.
+//                      covers elements 8w..8w+7, element i's 4-bit code
+//                      starting at bit nibble_pos(i) and wrapping past bit
+//                      31 to bit 0 (see the dequantisation in gemm_tc.cu).
 //   bytes [8192, 9216) scales: 128 rows x 4 groups of fp16, row r group g
 //                      at byte 8192 + (r*4 + g)*2.
 // Block index = (e * tiles_per_expert + tile) * k_chunks + chunk.
@@ -33,9 +34,14 @@ constexpr int kCodeBlockBytes = kTileRows * kChunkK / 2;       // 8192
 constexpr int kScaleBlockBytes = kTileRows * (kChunkK / kGroup) * 2;  // 1024
 constexpr int kBlockBytes = kCodeBlockBytes + kScaleBlockBytes;       // 9216
 constexpr int kHeaderBytes = 256;
+// Bit offset of element i's code inside its 32-bit word: 6, 22, 10, 26, 14,
+// 30, 18, 2 for i = 0..7.
+__host__ __device__ constexpr int nibble_pos(int i) {
+    return (((i & 1) ? 22 : 6) + 4 * (i >> 1)) & 31;
+}
 
 constexpr uint32_t kPackMagic = 0x5034574Du;  // "MW4P"
-constexpr uint32_t kPackVersion = 2;  // 2: codes and scales in one block
+constexpr uint32_t kPackVersion = 3;  // 3: one block per chunk, codes at nibble_pos
 
 struct PackHeader {
     uint32_t magic;
@@ -44,7 +50,8 @@ struct PackHeader {
     uint32_t block_bytes;  // kBlockBytes
     int32_t E, N, K, group;
     int32_t status;   // MOE_OK once the prepack finished and validated
-    int32_t pad[3];
+    int32_t wide_scales;  // nonzero: some |scale| > 65504/24 or infinite
+    int32_t pad[2];
 };
 static_assert(sizeof(PackHeader) <= kHeaderBytes, "header too large");
 
@@ -114,7 +121,8 @@ cudaError_t launch_align(const AlignArgs &a, cudaStream_t s);
 cudaError_t launch_prepack_codes(int kind, const uint8_t *q, int E, int N, int K,
                                  uint8_t *dst, cudaStream_t s);
 cudaError_t launch_prepack_scales(int kind, const uint16_t *sc, int E, int N, int K,
-                                  uint8_t *dst, int32_t *bad_flag, cudaStream_t s);
+                                  uint8_t *dst, int32_t *bad_flag, int32_t *wide_flag,
+                                  cudaStream_t s);
 
 struct GatherArgs {
     const uint16_t *hidden;  // [M][H] bf16

@@ -37,13 +37,13 @@ __global__ void prepack_codes_kernel(int kind, const uint32_t *__restrict__ q, i
         const int n = canonical_row(kind, N, tile, r);
         const int kk0 = chunk * kChunkK + pc * 32 + wi * 8;
         const uint32_t c = __ldg(q + (e * N + n) * row_words + kk0 / 8);
-        // canonical nibble i holds element i; output order 0,2,4,6,1,3,5,7
+        // canonical nibble i holds element i; it moves to bit nibble_pos(i)
+        // (a rotation, so the code at bit 30 wraps into bits 0-1)
         uint32_t o = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const uint32_t v = (c >> (4 * i)) & 0xFu;
-            const int slot = (i & 1) ? 4 + (i >> 1) : (i >> 1);
-            o |= v << (4 * slot);
+            o |= __funnelshift_l(v, v, nibble_pos(i));
         }
         reinterpret_cast<uint32_t *>(blocks + b * kBlockBytes)[wib] = o;
     }
@@ -51,9 +51,12 @@ __global__ void prepack_codes_kernel(int kind, const uint32_t *__restrict__ q, i
 
 // One thread per output fp16 scale (the last 1 KiB of a block).  A scale
 // must be zero, NaN, infinite or of magnitude in [2^-14, 8188] so that
-// (q - 8) * scale is exact in fp16.
+// (q - 8) * scale is exact in fp16.  Scales above 65504/24 in magnitude or
+// infinite set *wide_flag: the one-instruction dequantisation needs -24 * s
+// in fp16.
 __global__ void prepack_scales_kernel(int kind, const uint16_t *__restrict__ s, int E, int N,
-                                      int K, uint8_t *__restrict__ blocks, int32_t *bad_flag) {
+                                      int K, uint8_t *__restrict__ blocks, int32_t *bad_flag,
+                                      int32_t *wide_flag) {
     const int tiles = N / kTileRows, chunks = K / kChunkK, groups = K / kGroup;
     const int per_block = kTileRows * (kChunkK / kGroup);
     const int64_t total = (int64_t)E * tiles * chunks * per_block;
@@ -71,6 +74,7 @@ __global__ void prepack_scales_kernel(int kind, const uint16_t *__restrict__ s, 
         const bool ok = (f == 0.0f) || isnan(f) || isinf(f) ||
                         (a >= 6.103515625e-05f && a <= 8188.0f);
         if (!ok) atomicExch(bad_flag, 1);
+        if (isinf(f) || 24.0f * a > 65504.0f) atomicExch(wide_flag, 1);
         reinterpret_cast<__half *>(blocks + b * kBlockBytes + kCodeBlockBytes)[within] =
             __float2half_rn(f);
     }
@@ -92,10 +96,10 @@ cudaError_t launch_prepack_codes(int kind, const uint8_t *q, int E, int N, int K
 }
 
 cudaError_t launch_prepack_scales(int kind, const uint16_t *sc, int E, int N, int K, uint8_t *dst,
-                                  int32_t *bad_flag, cudaStream_t s) {
+                                  int32_t *bad_flag, int32_t *wide_flag, cudaStream_t s) {
     const int64_t n = (int64_t)E * (N / kTileRows) * (K / kChunkK) * (kScaleBlockBytes / 2);
     prepack_scales_kernel<<<grid_for(n), 256, 0, s>>>(kind, sc, E, N, K, dst + kHeaderBytes,
-                                                      bad_flag);
+                                                      bad_flag, wide_flag);
     return cudaGetLastError();
 }
 

@@ -32,11 +32,14 @@ def bf16_dev_to_f64(t) -> np.ndarray:
 class DeviceLayer:
     """Host canonical weights of one layer plus their prepacked device copies."""
 
-    def __init__(self, layer: synth.Layer, seed: int = 0):
+    def __init__(self, layer: synth.Layer, seed: int = 0, weights=None):
+        """``weights``: canonical (w13, s13, w2, s2) to use instead of the
+        seeded ones."""
         import quantized_moe_expert_align_gb300 as moe
         self.layer = layer
         self.seed = seed
-        self.w13, self.s13, self.w2, self.s2 = synth.layer_weights(layer, seed)
+        self.w13, self.s13, self.w2, self.s2 = (weights if weights is not None
+                                                else synth.layer_weights(layer, seed))
         torch = torch_mod()
         q = to_dev(self.w13)
         s = to_dev(self.s13.view(np.int16))

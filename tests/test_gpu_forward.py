@@ -64,6 +64,34 @@ def test_duplicate_ids_and_ragged(toy_layer):
     gu.parity(gu.bf16_dev_to_f64(out), toy_layer.oracle(x, ids, w), "toy duplicates")
 
 
+def _bf16(v):
+    return synth.f32_to_bf16_bits(np.array([v], np.float32))[0]
+
+
+@pytest.mark.parametrize("which", ["w13", "w2"])
+def test_wide_and_zero_scales(gpu, which):
+    """A scale above 65504/24 (here 2800, on a group whose only nonzero
+    weight is one code 9, so the activations stay in fp16 range) moves that
+    matrix to the two-step dequantisation; zero scales give zero weights.
+    Both against the oracle."""
+    L = synth.TOY.layer
+    w13, s13, w2, s2 = (a.copy() for a in synth.layer_weights(L, 0))
+    codes, sc = (w13, s13) if which == "w13" else (w2, s2)
+    for e in range(L.E):
+        sc[e, 3, 0] = _bf16(2800.0)
+        codes[e, 3, :16] = np.array([0x89] + [0x88] * 15, np.uint8)  # q - 8 = 1, 0, 0, ...
+        sc[e, 5, :] = 0
+    dl = gu.DeviceLayer(L, 0, weights=(w13, s13, w2, s2))
+    M = 16
+    x = synth.hidden(M, L.H, seed=2)
+    ids, w = synth.routing(M, L, seed=2)
+    out, ws = dl.forward(x, ids, w)
+    import quantized_moe_expert_align_gb300 as moe
+    st, _ = moe.moe_w4a16_get_device_status(ws.buf)
+    assert st == moe.MOE_OK, moe.moe_status_string(st)
+    gu.parity(gu.bf16_dev_to_f64(out), dl.oracle(x, ids, w), f"wide scale in {which}")
+
+
 # ---- larger batches: the forward runs on the whole batch, the oracle on a sample
 @pytest.mark.parametrize("M", [256, 512, 1024])
 def test_plateau_e384_sampled(e384_layer, M):
