@@ -518,6 +518,10 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             float *slot = part + ((size_t)g * 2 + which) * (size_t)NT * kTileRows;
 #pragma unroll 1
             for (int c0 = 0; c0 < t.rows; c0 += 16) {
+                // valid token columns of this block of 16 (warp-uniform); the
+                // loops below stop there, so a tile with a few rows costs a
+                // few columns of work
+                const int nval = min(16, t.rows - c0);
                 // Sum of the issuers' accumulators (and, with stacked hi/lo
                 // rows, of both halves), always in the same order.
                 uint32_t v[16];
@@ -547,37 +551,41 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                         if (KIND == MOE_PACK_W13) {
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
+                                if (j >= nval) break;
                                 const float mine = __uint_as_float(v[j]);
                                 const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-                                if (c0 + j < t.rows) {
-                                    const float gte = (lane & 1) ? other : mine;
-                                    const float up = (lane & 1) ? mine : other;
-                                    const float act = gte / (1.0f + expf(-gte)) * up;
-                                    const __half hi = __float2half_rn(act);
-                                    const size_t o = (size_t)(t.p0 + c0 + j) * a.I +
-                                                     t.rt * (kTileRows / 2) + (r >> 1);
-                                    if (lane & 1) {
-                                        const __half lo = __float2half_rn(act - __half2float(hi));
-                                        a.act_lo[o] = __half_as_ushort(lo);
-                                    } else {
-                                        a.act_hi[o] = __half_as_ushort(hi);
-                                        if (fabsf(act) > 65504.0f && !isinf(act) && !isnan(act))
-                                            set_status(a.ctrl, MOE_ERR_DEVICE_FP16_RANGE, 1);
-                                    }
+                                const float gte = (lane & 1) ? other : mine;
+                                const float up = (lane & 1) ? mine : other;
+                                const float act = gte / (1.0f + expf(-gte)) * up;
+                                const __half hi = __float2half_rn(act);
+                                const size_t o = (size_t)(t.p0 + c0 + j) * a.I +
+                                                 t.rt * (kTileRows / 2) + (r >> 1);
+                                if (lane & 1) {
+                                    const __half lo = __float2half_rn(act - __half2float(hi));
+                                    a.act_lo[o] = __half_as_ushort(lo);
+                                } else {
+                                    a.act_hi[o] = __half_as_ushort(hi);
+                                    if (fabsf(act) > 65504.0f && !isinf(act) && !isnan(act))
+                                        set_status(a.ctrl, MOE_ERR_DEVICE_FP16_RANGE, 1);
                                 }
                             }
                         } else {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                if (c0 + j < t.rows)
-                                    a.y[(size_t)(t.p0 + c0 + j) * a.N + t.rt * kTileRows + r] =
-                                        __uint_as_float(v[j]);
+                            for (int j = 0; j < 16; ++j) {
+                                if (j >= nval) break;
+                                a.y[(size_t)(t.p0 + c0 + j) * a.N + t.rt * kTileRows + r] =
+                                    __uint_as_float(v[j]);
+                            }
                         }
                     }
                 } else {
+                    // partial sums of the valid columns (the reduction reads
+                    // no others)
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
+                    for (int j = 0; j < 16; ++j) {
+                        if (j >= nval) break;
                         slot[(size_t)(c0 + j) * kTileRows + r] = __uint_as_float(v[j]);
+                    }
                 }
             }
             tc_fence_before();
