@@ -143,9 +143,12 @@ __device__ __forceinline__ Tile decode_tile(const TcArgs &a, const Smem *sm, int
     }
     t.e = lo;
     const int tp0 = sm->tile_prefix[lo], tp1 = sm->tile_prefix[lo + 1];
-    const int local = tile - R * tp0, te = tp1 - tp0;
-    t.rt = local / te;
-    const int tt = local % te;
+    // within an expert, tiles run over the 128-row weight tiles of one token
+    // tile before moving to the next token tile
+    const int local = tile - R * tp0;
+    (void)tp1;
+    t.rt = local % R;
+    const int tt = local / R;
     t.p0 = sm->offsets[lo] + tt * NT;
     t.rows = min(NT, sm->offsets[lo + 1] - t.p0);
     return t;
@@ -265,9 +268,27 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     pdl_trigger();
 
     const uint32_t tb = sm->tmem_base;
-    const int64_t W = sm->bad ? 0 : (int64_t)sm->tile_prefix[a.E] * R * KC;
+    // Schedule.  With many tiles (at least 8 per CTA) each CTA takes whole
+    // tiles g, g + G, g + 2G, ...: the CTAs then work on neighbouring tiles
+    // at the same time, which share token rows (tiles of one token tile are
+    // consecutive), so the token rows are read from L2, not DRAM.  With few
+    // tiles the chunks are cut into equal contiguous shares (stream-K).
+    const int T = sm->bad ? 0 : sm->tile_prefix[a.E] * R;
+    const bool rr = T >= 8 * G;
+    const int64_t W = (sm->bad || rr) ? 0 : (int64_t)T * KC;
     const int64_t u_begin = range_begin(g, W, G), u_end = range_begin(g + 1, W, G);
-    const int my_chunks = (int)(u_end - u_begin);
+    const int my_chunks = rr ? (g < T ? (T - g + G - 1) / G : 0) * KC : (int)(u_end - u_begin);
+    const int tstep = rr ? G : 1;  // tile index step when a tile's K chunks are done
+    // tile and K chunk of this CTA's chunk number c
+    auto locate_chunk = [&](int c, int &tile, int &kc) {
+        if (rr) {
+            tile = g + (c / KC) * G;
+            kc = c % KC;
+        } else {
+            tile = (int)((u_begin + c) / KC);
+            kc = (int)((u_begin + c) % KC);
+        }
+    };
 
     if (warp >= kProducerWarp && warp < kMmaWarp) {
         // ---------------- TMA producers (the whole warp runs the loop, one
@@ -288,17 +309,16 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
         // expert reads again, stay in L2 (without the hint, at M = 1024 on
         // E = 384 the gate+up GEMM read 1.86x its weight bytes from DRAM).
         const uint64_t pol_w = policy_evict_first();
-        int c = pw, kc = 0, s = pw, p0 = 0;
+        int c = pw, kc = 0, s = pw, p0 = 0, tile = 0;
         uint32_t phase = 0;
-        int64_t tile = 0, blk0 = 0;
+        int64_t blk0 = 0;
         auto locate = [&]() {
-            const Tile t = decode_tile<NT>(a, sm, (int)tile);
+            const Tile t = decode_tile<NT>(a, sm, tile);
             blk0 = ((int64_t)t.e * R + t.rt) * KC;
             p0 = t.p0;
         };
         if (c < my_chunks) {
-            tile = (u_begin + c) / KC;
-            kc = (int)((u_begin + c) % KC);
+            locate_chunk(c, tile, kc);
             locate();
         }
         for (; c < my_chunks; c += NPROD) {
@@ -327,7 +347,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             if (kc >= KC) {
                 do {
                     kc -= KC;
-                    ++tile;
+                    tile += tstep;
                 } while (kc >= KC);
                 if (c + NPROD < my_chunks) locate();
             }
@@ -355,9 +375,10 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
         const uint64_t desc_base = sdesc_k_sw128(smem_u32(base));
         int c = 0, seg = 0;  // c: CTA-local index of the segment's first chunk
         bool ok = true;
-        for (int64_t u = u_begin; u < u_end && ok; ++seg) {
-            const int tile = (int)(u / KC), k0 = (int)(u % KC);
-            const int k1 = (int)min((int64_t)KC, k0 + (u_end - u));
+        while (c < my_chunks && ok) {
+            int tile, k0;
+            locate_chunk(c, tile, k0);
+            const int k1 = min(KC, k0 + (my_chunks - c));
             const Tile t = decode_tile<NT>(a, sm, tile);
             const int n_mma = kCat ? 2 * NT : max(16, (t.rows + 15) & ~15);
             const uint32_t idesc = idesc_f16_m128((uint32_t)n_mma);
@@ -414,7 +435,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             if (elect_one()) tc_commit(&sm->acc_full[acc]);
             __syncwarp();
             c = c_end;
-            u += k1 - k0;
+            ++seg;
         }
         // Every MMA issued has completed once `done` fires.
         if (elect_one()) {
@@ -497,9 +518,10 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         float *part = a.partials;
         int seg = 0;
-        for (int64_t u = u_begin; u < u_end; ++seg) {
-            const int tile = (int)(u / KC), k0 = (int)(u % KC);
-            const int k1 = (int)min((int64_t)KC, k0 + (u_end - u));
+        for (int c_seg = 0; c_seg < my_chunks; ++seg) {
+            int tile, k0;
+            locate_chunk(c_seg, tile, k0);
+            const int k1 = min(KC, k0 + (my_chunks - c_seg));
             const Tile t = decode_tile<NT>(a, sm, tile);
             const int acc = seg & 1;
             if (!warp_wait_bar(&sm->acc_full[acc], (seg >> 1) & 1, sm, a.ctrl, 6)) break;
@@ -507,14 +529,13 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             const uint32_t acc_addr = tb + lane_off + kAccBase + acc * MMAW * kAccCols;
             // with two issuers, the second one had a chunk here unless the
             // segment is a single chunk that fell to the first (and vice versa)
-            const int c_seg = (int)(u - u_begin);
             bool has[2] = {true, true};
             if (MMAW == 2 && k1 - k0 == 1) {
                 has[0] = (c_seg % 2 == 0);
                 has[1] = !has[0];
             }
             const bool whole = (k0 == 0 && k1 == KC);
-            const int which = (u == u_begin) ? 0 : 1;  // first or last segment of this CTA
+            const int which = (c_seg == 0) ? 0 : 1;  // first or last segment of this CTA
             float *slot = part + ((size_t)g * 2 + which) * (size_t)NT * kTileRows;
 #pragma unroll 1
             for (int c0 = 0; c0 < t.rows; c0 += 16) {
@@ -633,7 +654,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                     }
                 }
             }
-            u += k1 - k0;
+            c_seg += k1 - k0;
         }
     }
 
