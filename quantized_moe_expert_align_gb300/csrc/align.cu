@@ -121,9 +121,14 @@ __global__ void __launch_bounds__(kThreads, 1) align_kernel(AlignArgs a) {
         const int toff = block_exclusive_scan(tiles, warp_buf, &ttotal);
         if (tid < E) a.tile_prefix[tid] = toff;
         if (tid == 0) a.tile_prefix[E] = ttotal;
+        const int tiles2 = (tid < E) ? (c + a.token_tile2 - 1) / a.token_tile2 : 0;
+        int ttotal2 = 0;
+        const int toff2 = block_exclusive_scan(tiles2, warp_buf, &ttotal2);
+        if (tid < E) a.tile_prefix2[tid] = toff2;
+        if (tid == 0) a.tile_prefix2[E] = ttotal2;
         if (a.tickets) {
             for (int i = tid; i < ttotal * a.r1; i += kThreads) a.tickets[i] = 0;
-            for (int i = tid; i < ttotal * a.r2; i += kThreads) a.tickets[a.off2 + i] = 0;
+            for (int i = tid; i < ttotal2 * a.r2; i += kThreads) a.tickets[a.off2 + i] = 0;
         }
     }
     __syncthreads();

@@ -29,11 +29,17 @@ int pick_token_tile(int n, int E) {
     // beats 128 at 85 and 128 rows, 128 wins at 341; at 22 rows 32 beats 64.
     const int active = n < E ? (n > 0 ? n : 1) : E;
     const int avg = (n + active - 1) / active;
-    if (avg >= 256) return 128;
     const int want = avg + avg / 4;
     int nt = 16;
-    while (nt < want && nt < 64) nt <<= 1;
+    while (nt < want && nt < 128) nt <<= 1;
     return nt;
+}
+
+// The down GEMM's stage holds both halves (hi, lo) of its token rows, so a
+// 128-row tile leaves room for only two stages: it uses 64-row tiles there.
+int down_token_tile(int nt) {
+    static const bool forced = std::getenv("MOE_W4A16_TOKEN_TILE") != nullptr;
+    return (forced || nt <= 64) ? nt : 64;
 }
 
 AlignLayout align_layout(int, int, int) {
@@ -47,7 +53,9 @@ FwdLayout fwd_layout(int M, int k, int E, int H, int I) {
     const size_t n = (size_t)M * k;
     FwdLayout l;
     l.nt = pick_token_tile((int)n, E);
+    l.nt2 = down_token_tile(l.nt);
     l.max_tok_tiles = (int)(n / l.nt) + (n < (size_t)E ? (int)n : E) + 1;
+    l.max_tok_tiles2 = (int)(n / l.nt2) + (n < (size_t)E ? (int)n : E) + 1;
     l.grid = kMaxGrid;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -59,10 +67,12 @@ FwdLayout fwd_layout(int M, int k, int E, int H, int I) {
     l.counts = take((size_t)E * 4);
     l.offsets = take((size_t)(E + 1) * 4);
     l.tile_prefix = take((size_t)(E + 1) * 4);
+    l.tile_prefix2 = take((size_t)(E + 1) * 4);
     l.perm = take(n * 4);
     l.inv_perm = take(n * 4);
     // one ticket per (tile, epilogue warp)
-    l.tickets = take((size_t)l.max_tok_tiles * 4 * (2 * I / kTileRows + H / kTileRows) * 4);
+    l.tickets = take(((size_t)l.max_tok_tiles * (2 * I / kTileRows) +
+                      (size_t)l.max_tok_tiles2 * (H / kTileRows)) * 4 * 4);
     l.partials = take((size_t)l.grid * 2 * l.nt * kTileRows * 4);
     l.xs = take(n * H * 2);
     l.act_hi = take(n * I * 2);
@@ -253,6 +263,7 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     int32_t *counts = reinterpret_cast<int32_t *>(ws + L.counts);
     int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
     int32_t *tile_prefix = reinterpret_cast<int32_t *>(ws + L.tile_prefix);
+    int32_t *tile_prefix2 = reinterpret_cast<int32_t *>(ws + L.tile_prefix2);
     int32_t *perm = reinterpret_cast<int32_t *>(ws + L.perm);
     int32_t *inv_perm = reinterpret_cast<int32_t *>(ws + L.inv_perm);
     int32_t *tickets = reinterpret_cast<int32_t *>(ws + L.tickets);
@@ -264,8 +275,8 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     const int n = M * k;
     const int r1 = 4 * (2 * I / kTileRows), r2 = 4 * (H / kTileRows);  // tickets per token tile
 
-    AlignArgs al = {ids, n, E, L.nt, counts, offsets, perm, inv_perm, tile_prefix, ctrl,
-                    tickets, r1, r2, L.max_tok_tiles * r1};
+    AlignArgs al = {ids, n, E, L.nt, L.nt2, counts, offsets, perm, inv_perm, tile_prefix,
+                    tile_prefix2, ctrl, tickets, r1, r2, L.max_tok_tiles * r1};
     GatherArgs ga = {hidden, perm, offsets, n, k, H, E, xs, ctrl};
     TcArgs g1 = {};
     g1.w = static_cast<const uint8_t *>(w13);
@@ -285,6 +296,8 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     TcArgs g2 = g1;
     g2.w = static_cast<const uint8_t *>(w2);
     g2.tickets = tickets + L.max_tok_tiles * r1;
+    g2.tile_prefix = tile_prefix2;
+    g2.nt = L.nt2;
     g2.N = H;
     g2.K = I;
     g2.kind = MOE_PACK_W2;
@@ -293,7 +306,7 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
 
     CUtensorMap map_x, map_act;
     if (!make_token_map(&map_x, xs, n, H, L.nt) ||
-        !make_act_map(&map_act, act_hi, act_lo, n, I, L.nt, stacked_hi_lo(L.nt)))
+        !make_act_map(&map_act, act_hi, act_lo, n, I, L.nt2, stacked_hi_lo(L.nt2)))
         return MOE_ERR_CUDA;
 
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };

@@ -80,11 +80,13 @@ AlignLayout align_layout(int M, int k, int E);
 
 // Carving of the forward workspace.
 struct FwdLayout {
-    int nt;             // token rows per MMA tile
+    int nt;             // token rows per MMA tile of the gate+up GEMM
+    int nt2;            // token rows per MMA tile of the down GEMM (<= nt)
     int max_tok_tiles;  // bound on sum_e ceil(count_e / nt)
+    int max_tok_tiles2; // bound on sum_e ceil(count_e / nt2)
     int grid;           // most CTAs the GEMM kernels may use (partials are sized for it)
-    size_t ctrl, counts, offsets, tile_prefix, perm, inv_perm;
-    size_t tickets;     // int32 [max_tok_tiles * (2I/128 + H/128)]
+    size_t ctrl, counts, offsets, tile_prefix, tile_prefix2, perm, inv_perm;
+    size_t tickets;     // int32 [max_tok_tiles * 4 * 2I/128 + max_tok_tiles2 * 4 * H/128]
     size_t partials;    // fp32 [grid][2][nt][128]
     size_t xs;          // [n][H] fp16 hidden rows in sorted order
     size_t act_hi;      // [n][I] fp16
@@ -92,8 +94,10 @@ struct FwdLayout {
     size_t y;           // [n][H] fp32
     size_t total;
 };
-// Token rows per tile for a batch of n = M*k slots over E experts.
+// Token rows per tile for a batch of n = M*k slots over E experts: for the
+// gate+up GEMM, and for the down GEMM given the former.
 int pick_token_tile(int n, int E);
+int down_token_tile(int nt);
 FwdLayout fwd_layout(int M, int k, int E, int H, int I);
 
 // moe_w4a16_forward on a scratch buffer the caller of this function chose.
@@ -109,10 +113,11 @@ struct AlignArgs {
     const int32_t *ids;
     int n;            // M * k
     int E;
-    int token_tile;   // >0: also write tile_prefix for this tile width
-    int32_t *counts, *offsets, *perm, *inv_perm, *tile_prefix;
+    int token_tile;   // >0: also write tile_prefix for this tile width,
+    int token_tile2;  //     and tile_prefix2 for this one
+    int32_t *counts, *offsets, *perm, *inv_perm, *tile_prefix, *tile_prefix2;
     Ctrl *ctrl;
-    int32_t *tickets; // if non-null: zero tiles*r1 entries at 0 and tiles*r2 at off2
+    int32_t *tickets; // if non-null: zero tiles*r1 entries at 0 and tiles2*r2 at off2
     int r1, r2, off2;
 };
 cudaError_t launch_align(const AlignArgs &a, cudaStream_t s);
