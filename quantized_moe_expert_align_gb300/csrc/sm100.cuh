@@ -2,8 +2,9 @@
 // here for sm_103a) features the expert GEMMs use: mbarriers, TMA bulk and
 // tensor copies, tcgen05 tensor-memory allocation, loads/stores and MMA.
 //
-// Every wait is bounded: after kSpinLimit polls it gives up and reports
-// false, so a kernel can record an error and return instead of hanging.
+// The waits built on these (gemm_tc.cu) are bounded: they give up after a
+// fixed number of SM cycles, so a kernel can record an error and return
+// instead of hanging.
 #pragma once
 
 #include <cstdint>
@@ -12,8 +13,6 @@
 
 namespace moe {
 namespace sm100 {
-
-constexpr uint32_t kSpinLimit = 1u << 26;   // ~seconds of polling, then give up
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -70,44 +69,18 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
         : "memory");
     return ok != 0;
 }
-// Wait for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
-// Contiguous global -> shared copy; dst, src 16-byte aligned, bytes % 16 == 0.
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
-                                         uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-// 2-D tiled tensor copy global -> shared (box from the tensor map); x is the
-// innermost coordinate in elements and must be 16-byte aligned.
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int32_t x,
-                                            int32_t y, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
 // L2 eviction policy for streamed data that is read once.
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
-// bulk_g2s with an L2 eviction policy.
+// Contiguous global -> shared copy with an L2 eviction policy; dst, src
+// 16-byte aligned, bytes % 16 == 0; completes `bytes` on the mbarrier.
 __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes,
                                               uint64_t *bar, uint64_t policy) {
     asm volatile(
@@ -116,7 +89,9 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
-// 3-D and 4-D tiled tensor copies (same rules: x 16-byte aligned).
+// 3-D and 4-D tiled tensor copies global -> shared (box from the tensor
+// map); x is the innermost coordinate in elements and must be 16-byte
+// aligned.
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int32_t x,
                                             int32_t y, int32_t z, uint64_t *bar) {
     asm volatile(
@@ -167,14 +142,8 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// Store 8 consecutive 32-bit columns of this thread's TMEM lane (32x32b
+// Store 16 consecutive 32-bit columns of this thread's TMEM lane (32x32b
 // shape: thread t of the warp owns lane (warp quarter base + t)).
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-        : "memory");
-}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
