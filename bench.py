@@ -45,10 +45,10 @@ KERNELS = ["align", "gather", "gemm_gate_up", "gemm_down", "combine"]
 # given (see the profile named there).  For any other source the figure no
 # longer describes the kernel and the bench reports traffic as null.
 TRAFFIC_CAPTURE = {
-    "sources_sha256": "b075adf528e197e0110d1a8092e6d42dab50ea0b9261b91d7370f8e9caab3dba",
+    "sources_sha256": "ccf7490c19c4b8e521f1e9c34f58bfdd7edd72ff599d594b6340d15b4be59e99",
     "workload": "decode_e384_h7168_i2048_top8",
-    "bytes_per_launch": {1: 132318976 + 2956032, 9: 1091161088 + 1305088,
-                         90: 5559684352 + 2897408},
+    "bytes_per_launch": {1: 132322816 + 2745344, 9: 1091145728 + 888576,
+                         90: 5559526912 + 1867776},
     "profile": "profiles/dram_gemm_gate_up_decode_e384_m1_9_90.md",
 }
 KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "sm100.cuh", "moe_internal.h", "device_common.cuh"]
