@@ -202,6 +202,23 @@ __device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, __half2 c2,
     exact_pairs(rotr(w, 14), s2, o[2], o[3]);
 }
 
+// SiLU(gate) * up of one gate/up lane pair, as the fp16 pair hi + lo of
+// the lane's parity: hi = fp16(a) for even lanes, lo = fp16(a - hi) for odd
+// ones.  Both lanes compute a (no divergent branch); v is the lane's
+// accumulator value, the partner's comes over a shuffle.  __expf and
+// __fdividef (relative error ~1e-6) are far inside the layer tolerance.
+// Sets *overflow when a finite a is beyond fp16 range.
+__device__ __forceinline__ uint16_t silu_mul_half(float v, int lane, bool &overflow) {
+    const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+    const float gte = (lane & 1) ? other : v;
+    const float up = (lane & 1) ? v : other;
+    const float act = __fdividef(gte * up, 1.0f + __expf(-gte));
+    const __half hi = __float2half_rn(act);
+    const __half lo = __float2half_rn(act - __half2float(hi));
+    overflow |= fabsf(act) > 65504.0f && fabsf(act) < INFINITY;
+    return __half_as_ushort((lane & 1) ? lo : hi);
+}
+
 template <int KIND, int NT, int STAGES, int DQG, int NPROD, int MMAW>
 __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     gemm_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tok) {
@@ -570,26 +587,19 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                 if (whole) {
                     {
                         if (KIND == MOE_PACK_W13) {
+                            // even lanes write hi, odd lanes lo, of act
+                            // column rt*64 + r/2
+                            uint16_t *dst = ((lane & 1) ? a.act_lo : a.act_hi) +
+                                            (size_t)(t.p0 + c0) * a.I + t.rt * (kTileRows / 2) +
+                                            (r >> 1);
+                            bool overflow = false;
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
                                 if (j >= nval) break;
-                                const float mine = __uint_as_float(v[j]);
-                                const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-                                const float gte = (lane & 1) ? other : mine;
-                                const float up = (lane & 1) ? mine : other;
-                                const float act = gte / (1.0f + expf(-gte)) * up;
-                                const __half hi = __float2half_rn(act);
-                                const size_t o = (size_t)(t.p0 + c0 + j) * a.I +
-                                                 t.rt * (kTileRows / 2) + (r >> 1);
-                                if (lane & 1) {
-                                    const __half lo = __float2half_rn(act - __half2float(hi));
-                                    a.act_lo[o] = __half_as_ushort(lo);
-                                } else {
-                                    a.act_hi[o] = __half_as_ushort(hi);
-                                    if (fabsf(act) > 65504.0f && !isinf(act) && !isnan(act))
-                                        set_status(a.ctrl, MOE_ERR_DEVICE_FP16_RANGE, 1);
-                                }
+                                dst[(size_t)j * a.I] =
+                                    silu_mul_half(__uint_as_float(v[j]), lane, overflow);
                             }
+                            if (overflow) set_status(a.ctrl, MOE_ERR_DEVICE_FP16_RANGE, 1);
                         } else {
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
@@ -634,20 +644,11 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                             if (range_begin(gg + 1, W, G) > tu1) break;
                         }
                         if (KIND == MOE_PACK_W13) {
-                            const float other = __shfl_xor_sync(0xffffffffu, sum, 1);
-                            const float gte = (lane & 1) ? other : sum;
-                            const float up = (lane & 1) ? sum : other;
-                            const float act = gte / (1.0f + expf(-gte)) * up;
-                            const __half hi = __float2half_rn(act);
-                            const size_t o = (size_t)(t.p0 + col) * a.I + t.rt * (kTileRows / 2) +
-                                             (r >> 1);
-                            if (lane & 1) {
-                                a.act_lo[o] = __half_as_ushort(__float2half_rn(act - __half2float(hi)));
-                            } else {
-                                a.act_hi[o] = __half_as_ushort(hi);
-                                if (fabsf(act) > 65504.0f && !isinf(act) && !isnan(act))
-                                    set_status(a.ctrl, MOE_ERR_DEVICE_FP16_RANGE, 1);
-                            }
+                            bool overflow = false;
+                            const uint16_t val = silu_mul_half(sum, lane, overflow);
+                            ((lane & 1) ? a.act_lo : a.act_hi)[(size_t)(t.p0 + col) * a.I +
+                                                               t.rt * (kTileRows / 2) + (r >> 1)] = val;
+                            if (overflow) set_status(a.ctrl, MOE_ERR_DEVICE_FP16_RANGE, 1);
                         } else {
                             a.y[(size_t)(t.p0 + col) * a.N + t.rt * kTileRows + r] = sum;
                         }
