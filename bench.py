@@ -134,6 +134,24 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def max_over_ranks(value, device="cpu"):
+    """The largest of every rank's ``value`` (the job's time is its slowest
+    replica's); ``value`` itself without an initialised multi-rank group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(tokens_per_step, steps, world, ms):
+    """Whole-job tokens/s: every replica processed the same tokens in at
+    most ``ms`` (max over ranks)."""
+    return world * tokens_per_step * steps / (ms / 1e3)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -299,13 +317,9 @@ def our_arm(args, wl):
     step_ms = [m[0].elapsed_time(m[nM]) for m in marks]
     call_ms = {M: float(np.mean([m[j].elapsed_time(m[j + 1]) for m in marks]))
                for j, M in enumerate(wl.Ms)}
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), "cuda")
     tokens_per_step = sum(wl.Ms)
-    value = world * tokens_per_step * args.steps / (total_ms / 1e3)
+    value = job_value(tokens_per_step, args.steps, world, total_ms)
     gpu_launches = moe.moe_w4a16_get_diag()["kernels_launched"] * len(wl.Ms) * args.steps
 
     # ---- per-kernel durations (events between the library's kernels) ----
@@ -381,12 +395,8 @@ def our_arm(args, wl):
             hout.copy_(out.view(torch.int16), non_blocking=True)
         e_en[i].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_st, e_en))
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * tokens_per_step * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(e_st, e_en)), "cuda")
+    e2e = {"value": job_value(tokens_per_step, args.steps, world, e2e_ms), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     cpu = None
