@@ -1,0 +1,79 @@
+"""Layer shapes beyond the workloads, against the oracle: the largest E the
+library takes (1024, with enough tiles for the round-robin whole-tile
+schedule), every expert selected (k = E = 64), odd tile and chunk counts
+(H = 384: three 128-row tiles of the down GEMM and three K chunks of the
+gate+up GEMM; I = 128: one K chunk of the down GEMM), and the 128-row token
+tile of the down GEMM, which the library only picks when told to."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import synth
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(L, M, seed=0, sample=None):
+    import quantized_moe_expert_align_gb300 as moe
+    dl = gu.DeviceLayer(L, seed)
+    x = synth.hidden(M, L.H, seed)
+    ids, w = synth.routing(M, L, seed)
+    out, ws = dl.forward(x, ids, w)
+    st, _ = moe.moe_w4a16_get_device_status(ws.buf)
+    assert st == moe.MOE_OK, moe.moe_status_string(st)
+    got = gu.bf16_dev_to_f64(out)
+    rows = None if sample is None else gu.sample_rows(M, sample)
+    ref = dl.oracle(x, ids, w, rows)
+    return gu.parity(got if rows is None else got[rows], ref, f"E{L.E} H{L.H} I{L.I} k{L.k} M{M}")
+
+
+def test_e1024_round_robin(gpu):
+    import quantized_moe_expert_align_gb300 as moe
+    L = synth.Layer(1024, 256, 128, 8)
+    _run(L, 2048, sample=48)
+    assert moe.moe_w4a16_get_diag()["token_tile"] == 32
+
+
+def test_every_expert_selected(gpu):
+    _run(synth.Layer(64, 256, 128, 64), 24)
+
+
+@pytest.mark.parametrize("M", [3, 200])
+def test_odd_tiles_and_chunks(gpu, M):
+    _run(synth.Layer(16, 384, 128, 4), M)
+
+
+_CHILD = r"""
+import json, sys
+sys.path.insert(0, sys.argv[1])
+import synth
+from tests import gpu_util as gu
+import quantized_moe_expert_align_gb300 as moe
+L = synth.Layer(32, 256, 256, 8)
+M = 600
+dl = gu.DeviceLayer(L, 0)
+x = synth.hidden(M, L.H, 0)
+ids, w = synth.routing(M, L, 0)
+out, ws = dl.forward(x, ids, w)
+st, _ = moe.moe_w4a16_get_device_status(ws.buf)
+ratio, rel = gu.parity(gu.bf16_dev_to_f64(out), dl.oracle(x, ids, w), "forced 128")
+print(json.dumps({"status": st, "tile": moe.moe_w4a16_get_diag()["token_tile"],
+                  "ratio": ratio, "rel": rel}))
+"""
+
+
+def test_forced_128_row_tiles(gpu):
+    """Both GEMMs on 128-row token tiles (the down GEMM's separate hi and lo
+    MMAs); the tile choice is read once per process, so in a child."""
+    env = dict(os.environ, MOE_W4A16_TOKEN_TILE="128")
+    r = subprocess.run([sys.executable, "-c", _CHILD, ROOT], env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    assert res["status"] == 0 and res["tile"] == 128
