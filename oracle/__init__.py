@@ -64,6 +64,8 @@ class Oracle:
         lib.oracle_dequant_element.argtypes = [p, p, i64, i64, i64]
         lib.oracle_align.restype = i64
         lib.oracle_align.argtypes = [p, i64, i64, i64, p, p, p, p]
+        lib.oracle_route.restype = i64
+        lib.oracle_route.argtypes = [p, i64, i64, i64, p, p]
         lib.oracle_forward.restype = i64
         lib.oracle_forward.argtypes = [p, p, p, p, p, p, p,
                                        i64, i64, i64, i64, i64,
@@ -97,6 +99,20 @@ class Oracle:
                                     _ptr(perm), _ptr(inv_perm))
         n = M * k
         return counts, offsets, perm[:n], inv_perm[:n], int(bad)
+
+    def route(self, logits, k: int):
+        """Softmax top-k router with renormalised weights.
+
+        ``logits`` [M][E] fp32.  Returns (ids [M][k] int32, topk_w [M][k]
+        fp32, bad_rows); a bad row (NaN or +inf logit) has zero weights.
+        """
+        logits = np.ascontiguousarray(logits, dtype=np.float32)
+        M, E = logits.shape
+        assert 1 <= k <= E
+        ids = np.full((M, k), -1, np.int32)
+        w = np.zeros((M, k), np.float32)
+        bad = self.lib.oracle_route(_ptr(logits), M, E, k, _ptr(ids), _ptr(w))
+        return ids, w, int(bad)
 
     def forward(self, hidden, ids, topk_w, w13, s13, w2, s2, E: int, H: int, I: int,
                 want_intermediates: bool = False):
@@ -157,6 +173,10 @@ def dequant_element(q, s, n, kk):
 
 def align(ids, E):
     return default().align(ids, E)
+
+
+def route(logits, k):
+    return default().route(logits, k)
 
 
 def forward(*args, **kwargs):

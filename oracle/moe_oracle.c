@@ -39,7 +39,10 @@
  *  - out[t] = sum over j = 0..k-1 ascending of topk_w[t][j] * y(t, j), with no
  *    renormalisation of topk_w;
  *  - a slot whose expert id lies outside [0, E) is left out of the alignment
- *    (inv_perm = -1) and contributes zero.
+ *    (inv_perm = -1) and contributes zero;
+ *  - the router (oracle_route, ahead of the layer): softmax over the E
+ *    logits, top-k by descending value with ties to the lower expert index,
+ *    weights renormalised to sum 1 over the k selected.
  *
  * Parity status: every function here is pinned by the CPU tests (worked
  * byte/scale fixtures, closed forms, a brute-force dense per-token path,
@@ -215,4 +218,79 @@ int64_t oracle_forward(const uint16_t *hidden, const int32_t *ids,
         }
     }
     return invalid;
+}
+
+/*
+ * Router front-end (the step that produces topk_ids and topk_w from the
+ * router's logits).  The pages do not describe the router; the reading used
+ * is the usual softmax top-k with renormalisation:
+ *   p[e] = exp(l[e]) / sum_e' exp(l[e'])              (softmax over all E)
+ *   ids[t][0..k-1] = the k experts of largest p, in descending order, the
+ *                    lower expert index first among equal values
+ *   w[t][j] = p[ids[t][j]] / sum_{j' < k} p[ids[t][j']]   (renormalised)
+ * The softmax is monotone, so the order is taken on the logits themselves,
+ * compared as numbers (-0 equals +0).  Inputs outside the ordinary range:
+ *  - a logit of -inf has p = 0 and ranks after every finite logit;
+ *  - NaN ranks after everything else (lower index first among NaNs);
+ *  - a row holding a NaN or +inf has no softmax: its ids still follow the
+ *    order above, its weights are all 0, and it is counted as a bad row;
+ *  - a row whose logits are all -inf has weights all 0 (not a bad row).
+ * Arithmetic in double; the weights are rounded once to fp32.
+ * Returns the number of bad rows.
+ */
+
+/* 1 when logit a of expert ea comes before logit b of expert eb. */
+static int ranks_before(float a, int64_t ea, float b, int64_t eb)
+{
+    int an = isnan(a), bn = isnan(b);
+    if (an != bn) return bn;           /* the number comes first */
+    if (!an && a != b) return a > b;   /* larger first; -0 == +0 */
+    return ea < eb;                    /* equal (or both NaN): lower index */
+}
+
+int64_t oracle_route(const float *logits, int64_t M, int64_t E, int64_t k,
+                     int32_t *ids, float *topk_w)
+{
+    int64_t bad_rows = 0;
+#pragma omp parallel for schedule(static) reduction(+ : bad_rows)
+    for (int64_t t = 0; t < M; ++t) {
+        const float *l = logits + t * E;
+        int32_t *id = ids + t * k;
+        float *w = topk_w + t * k;
+
+        /* selection: k passes, each taking the first-ranked expert not yet
+         * taken */
+        for (int64_t j = 0; j < k; ++j) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; ++e) {
+                int taken = 0;
+                for (int64_t i = 0; i < j; ++i)
+                    if (id[i] == e) taken = 1;
+                if (taken) continue;
+                if (best < 0 || ranks_before(l[e], e, l[best], best)) best = e;
+            }
+            id[j] = (int32_t)best;
+        }
+
+        int bad = 0;
+        double mx = -INFINITY;
+        for (int64_t e = 0; e < E; ++e) {
+            if (isnan(l[e]) || (isinf(l[e]) && l[e] > 0)) bad = 1;
+            else if ((double)l[e] > mx) mx = (double)l[e];
+        }
+        if (bad || mx == -INFINITY) {
+            for (int64_t j = 0; j < k; ++j) w[j] = 0.0f;
+            bad_rows += bad;
+            continue;
+        }
+        /* softmax over all E (shifted by the maximum, which leaves it
+         * unchanged), then renormalised over the selected k */
+        double z = 0.0;
+        for (int64_t e = 0; e < E; ++e) z += exp((double)l[e] - mx);
+        double sel = 0.0;
+        for (int64_t j = 0; j < k; ++j) sel += exp((double)l[id[j]] - mx) / z;
+        for (int64_t j = 0; j < k; ++j)
+            w[j] = (float)((exp((double)l[id[j]] - mx) / z) / sel);
+    }
+    return bad_rows;
 }

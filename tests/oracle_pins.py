@@ -17,7 +17,12 @@ What each pin rests on:
     grouping, numpy matmul) on tiny random layers;
   * special cases -- all-zero codes give exactly zero, k = 1 with weight 1 is a
     single-expert MLP, outputs are linear in topk_w and equivariant under
-    token permutation, unused experts are never read.
+    token permutation, unused experts are never read;
+  * router        -- the selection equals a Python sort by (-logit, index) on
+    tie-heavy inputs; the weights equal a full numpy softmax renormalised
+    over the selection, and closed forms (equal logits give 1/k; logits
+    -e ln 2 give 2^-j / (2 - 2^(1-k))); NaN / +inf / -inf rows follow the
+    stated rules.
 """
 from __future__ import annotations
 
@@ -294,7 +299,98 @@ def check_forward_invalid_slot_contributes_zero(orc):
     assert np.all(out[2] != 0.0)
 
 
-ALL_PINS = [check_dequant_worked_bytes, check_align_matches_stable_sort,
+def _py_topk(row, k):
+    """Order by descending logit, lower index first on ties, NaN last."""
+    def key(e):
+        v = float(row[e])
+        return (1, 0.0, e) if math.isnan(v) else (0, -v, e)
+    return sorted(range(len(row)), key=key)[:k]
+
+
+def check_route_selection_brute_force(orc):
+    rng = np.random.default_rng(23)
+    for trial in range(60):
+        E = int(rng.integers(1, 41))
+        k = int(rng.integers(1, E + 1))
+        M = int(rng.integers(1, 6))
+        # few distinct values, so ties are common; signed zeros compare equal
+        vals = np.array([-1.5, -0.0, 0.0, 0.25, 1.0, 1.0], np.float32)
+        lg = vals[rng.integers(0, len(vals), size=(M, E))]
+        ids, _, bad = orc.route(lg, k)
+        assert bad == 0
+        for t in range(M):
+            assert list(ids[t]) == _py_topk(lg[t], k), (trial, t)
+
+
+def check_route_weights_full_softmax(orc):
+    rng = np.random.default_rng(29)
+    for E, k, M in [(8, 2, 5), (64, 8, 7), (384, 8, 4), (17, 17, 3), (128, 1, 3)]:
+        lg = (rng.standard_normal((M, E)) * 3).astype(np.float32)
+        ids, w, bad = orc.route(lg, k)
+        assert bad == 0
+        x = lg.astype(np.float64)
+        p = np.exp(x - x.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        for t in range(M):
+            assert list(ids[t]) == _py_topk(lg[t], k)
+            sel = p[t, ids[t]]
+            ref = sel / sel.sum()
+            assert np.all(np.abs(w[t] - ref) <= 2.0 ** -23 * ref), (E, k, t)
+            assert np.all(np.diff(w[t].astype(np.float64)) <= 0)
+
+
+def check_route_closed_forms(orc):
+    # equal logits: the first k experts, each 1/k
+    for E, k in [(8, 2), (384, 8), (5, 5), (3, 1)]:
+        ids, w, _ = orc.route(np.full((2, E), 0.75, np.float32), k)
+        assert np.array_equal(ids, np.tile(np.arange(k, dtype=np.int32), (2, 1)))
+        assert np.all(w == np.float32(1.0 / k))
+    # logits -e ln 2: p_e proportional to 2^-e, so w_j = 2^-j / (2 - 2^(1-k))
+    E = 40
+    lg = (-np.arange(E) * math.log(2.0)).astype(np.float32)[None, :]
+    for k in (1, 2, 8, 20):
+        ids, w, _ = orc.route(lg, k)
+        assert np.array_equal(ids[0], np.arange(k))
+        ref = np.array([2.0 ** -j / (2.0 - 2.0 ** (1 - k)) for j in range(k)])
+        assert np.all(np.abs(w[0] - ref) <= 1e-6 * ref), k
+    # one dominant logit: weight 1 on it, 0 elsewhere (exp underflows)
+    lg = np.zeros((1, 16), np.float32)
+    lg[0, 11] = 1000.0
+    ids, w, _ = orc.route(lg, 3)
+    assert list(ids[0]) == [11, 0, 1] and list(w[0]) == [1.0, 0.0, 0.0]
+
+
+def check_route_special_values(orc):
+    inf, nan = np.inf, np.nan
+    lg = np.array([[0.5, -inf, 2.0, -inf, 1.0],     # -inf: weight 0, ranked after numbers
+                   [nan, 1.0, nan, 0.0, -inf],      # NaN: bad row, ranked last
+                   [0.0, inf, 1.0, 2.0, 3.0],       # +inf: bad row, ranked first
+                   [-inf, -inf, -inf, -inf, -inf]], # all -inf: zero weights, not bad
+                  np.float32)
+    ids, w, bad = orc.route(lg, 4)
+    assert bad == 2
+    assert list(ids[0]) == [2, 4, 0, 1] and w[0, 3] == 0.0 and w[0, 2] > 0
+    assert abs(float(w[0].astype(np.float64).sum()) - 1.0) <= 4 * 2.0 ** -24
+    assert list(ids[1]) == [1, 3, 4, 0] and np.all(w[1] == 0)
+    assert list(ids[2]) == [1, 4, 3, 2] and np.all(w[2] == 0)
+    assert list(ids[3]) == [0, 1, 2, 3] and np.all(w[3] == 0)
+
+
+def check_route_matches_input_generator(orc):
+    # synth.route draws the workloads' routing with numpy (stable argsort,
+    # softmax over the selected logits): an independent implementation
+    for M, E, k, zipf in [(64, 384, 8, None), (64, 384, 8, 1.1), (16, 8, 2, None)]:
+        lg = synth.logits(M, E, seed=3, zipf_s=zipf)
+        ids, w, bad = orc.route(lg, k)
+        ids_ref, w_ref = synth.route(lg, k)
+        assert bad == 0 and np.array_equal(ids, ids_ref)
+        assert np.all(np.abs(w - w_ref) <= 2.0 ** -23 * w_ref)
+
+
+ALL_PINS = [check_route_selection_brute_force, check_route_weights_full_softmax,
+            check_route_closed_forms, check_route_special_values,
+            check_route_matches_input_generator,
+            check_dequant_worked_bytes, check_align_matches_stable_sort,
             check_align_invalid_ids, check_forward_closed_form,
             check_forward_brute_force, check_forward_zero_codes,
             check_forward_single_expert_mlp, check_forward_linearity_and_permutation,

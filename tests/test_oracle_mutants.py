@@ -1,7 +1,7 @@
 """Plant plausible mistakes in copies of the oracle source and require the
 pins to catch every one.  This shows the pins constrain each part of the
-oracle: dequantisation, alignment, both projections, the activation and the
-combine."""
+oracle: dequantisation, alignment, both projections, the activation, the
+combine and the router."""
 import os
 
 import pytest
@@ -29,6 +29,14 @@ MUTANTS = [
     ("unstable placement", "int32_t pos = offsets[e] + counts[e];",
      "int32_t pos = offsets[e + 1] - 1 - counts[e];"),
     ("token index from slot modulo", "int64_t t = f / k;", "int64_t t = f % k;"),
+    ("router ties to the higher index", "return ea < eb;", "return ea > eb;"),
+    ("router NaN ranked first", "if (an != bn) return bn;", "if (an != bn) return an;"),
+    ("router ascending order", "return a > b;", "return a < b;"),
+    ("router weights not renormalised", "/ z) / sel);", "/ z));"),
+    ("router softmax without shift", "z += exp((double)l[e] - mx);", "z += exp((double)l[e]);"),
+    ("router bad rows kept", "if (bad || mx == -INFINITY)", "if (mx == -INFINITY)"),
+    ("router weight of the top slot everywhere", "(float)((exp((double)l[id[j]] - mx)",
+     "(float)((exp((double)l[id[0]] - mx)"),
 ]
 
 
