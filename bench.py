@@ -339,6 +339,47 @@ def our_arm(args, wl):
     for M in wl.Ms:
         per_kernel[M] /= prof_steps
 
+    # ---- router front-end: logits -> ids, weights and alignment alone
+    # (moe_route_align), and the whole layer from logits
+    # (moe_w4a16_forward_routed); same logits as the batches' routing ----
+    router = {}
+    for M in wl.Ms:
+        x, ids, w, out = devb[M]
+        lg = dev(synth.logits(M, L.E, seed=0, zipf_s=wl.zipf_s))
+        r_ids = torch.empty((M, L.k), dtype=torch.int32, device="cuda")
+        r_w = torch.empty((M, L.k), dtype=torch.float32, device="cuda")
+        cnt = torch.empty(L.E, dtype=torch.int32, device="cuda")
+        off = torch.empty(L.E + 1, dtype=torch.int32, device="cuda")
+        perm = torch.empty(M * L.k, dtype=torch.int32, device="cuda")
+        inv = torch.empty(M * L.k, dtype=torch.int32, device="cuda")
+        aws = torch.empty(max(moe.moe_align_workspace_size(M, L.k, L.E), 256),
+                          dtype=torch.uint8, device="cuda")
+        t_route = t_layer = 0.0
+        for _ in range(prof_steps):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            flush.zero_()
+            evs[0].record(stream)
+            st = moe.moe_route_align(lg, M, L.k, L.E, r_ids, r_w, cnt, off, perm, inv, aws, stream)
+            evs[1].record(stream)
+            st2 = moe.moe_w4a16_forward_routed(x, lg, p13, p2, out, r_ids, r_w, M, L.k, L.E,
+                                               L.H, L.I, ws.buf, stream)
+            evs[2].record(stream)
+            if st != moe.MOE_OK or st2 != moe.MOE_OK:
+                raise moe.MoeError(st or st2, "router front-end")
+            torch.cuda.synchronize()
+            t_route += evs[0].elapsed_time(evs[1]) / prof_steps
+            t_layer += evs[1].elapsed_time(evs[2]) / prof_steps
+        st, detail = moe.moe_w4a16_get_device_status(ws.buf)
+        if st != moe.MOE_OK:
+            raise moe.MoeError(st, f"routed forward device status (detail {detail})")
+        if not torch.equal(r_ids, ids):
+            raise RuntimeError(f"routed ids differ from the batch's routing at M={M}")
+        nbytes = M * L.E * 4 + M * L.k * 8
+        router[M] = {"route_align_us": round(1e3 * t_route, 2),
+                     "route_bytes": nbytes,
+                     "route_gbs": round(nbytes / (t_route / 1e3) / 1e9, 1),
+                     "us_per_call_from_logits": round(1e3 * t_layer, 2)}
+
     # roofline: the gate+up GEMM streams the touched experts' w13 codes+scales
     b13, b2 = expert_bytes(L)
     sweep = []
@@ -360,6 +401,7 @@ def our_arm(args, wl):
             "roofline_bytes": roof_bytes, "roofline_us": round(1e3 * t_roof_ms, 2),
             "frac_of_roofline_profiled": round(t_roof_ms / float(k_ms.sum()), 4),
             "pages_ms_rtx_pro_6000": PAGES_MS.get(M) if L.E == 384 else None,
+            "router": router[M],
         })
     achieved = gemm1_bytes / (gemm1_ms / 1e3) / 1e9
     traffic = None

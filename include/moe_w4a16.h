@@ -30,8 +30,9 @@
  *    workspace, no sm_103 device) return before anything is launched.
  *  - Errors found on the device (an expert id outside [0, E), a prepacked
  *    buffer whose header does not match, an activation beyond fp16 range,
- *    a bounded wait that ran out) never trap: the kernels record the first
- *    one in the workspace's status word and skip the affected work.
+ *    a NaN or +inf router logit, a bounded wait that ran out) never trap:
+ *    the kernels record the first one in the workspace's status word and
+ *    skip the affected work.
  *    moe_w4a16_get_device_status() reads it back.  Each forward or align
  *    call resets the word when it starts.
  *  - A workspace must not be used by two calls that overlap on the GPU.
@@ -59,7 +60,8 @@ typedef enum {
     MOE_ERR_CUDA = 6,                 /* a CUDA runtime call failed */
     MOE_ERR_DEVICE_BAD_EXPERT_ID = 7, /* an id outside [0, E) was seen */
     MOE_ERR_DEVICE_TIMEOUT = 8,       /* a bounded device wait gave up */
-    MOE_ERR_DEVICE_FP16_RANGE = 9     /* a value is not representable in fp16 */
+    MOE_ERR_DEVICE_FP16_RANGE = 9,    /* a value is not representable in fp16 */
+    MOE_ERR_DEVICE_BAD_LOGIT = 10     /* a router logit is NaN or +inf */
 } moe_status_t;
 
 /* Which matrix a prepacked buffer holds. */
@@ -132,6 +134,35 @@ moe_status_t moe_align(const int32_t *topk_ids, int M, int k, int E,
                        int32_t *inv_perm, void *workspace, size_t ws_bytes,
                        moe_stream_t stream);
 
+/*
+ * Router front-end fused with the alignment: from the router's logits, the
+ * top-k experts of every token and their renormalised softmax weights, then
+ * the alignment of those ids exactly as moe_align.  The pages do not
+ * describe the router; the definition is that of the layer's benchmark
+ * inputs, a softmax over all E logits, its k largest, weights renormalised
+ * to sum 1:
+ *   topk_ids[t][0..k-1] = experts in descending logit order, the lower
+ *                         expert index first among equal logits (-0 == +0;
+ *                         -inf after every number; NaN after everything);
+ *   topk_w[t][j] = exp(l_j - l_0) / sum_{i<k} exp(l_i - l_0), l_j the logit
+ *                  of slot j (the softmax normaliser over all E cancels).
+ *
+ *  logits   [M][E] fp32, device, 4-byte aligned.
+ *  topk_ids [M][k] int32, topk_w [M][k] fp32, device, out.
+ *  counts, offsets, perm, inv_perm, workspace: as in moe_align
+ *           (workspace of moe_align_workspace_size bytes).
+ * Limits: those of moe_align and k <= E.  A row holding a NaN or +inf logit
+ * keeps ids in the order above, gets all-zero weights, and is reported as
+ * MOE_ERR_DEVICE_BAD_LOGIT (detail = its token index); a row of only -inf
+ * logits gets all-zero weights.  Batches of at most 64 tokens are routed
+ * inside the alignment kernel (one launch); larger ones by a separate
+ * kernel first.
+ */
+moe_status_t moe_route_align(const float *logits, int M, int k, int E,
+                             int32_t *topk_ids, float *topk_w, int32_t *counts,
+                             int32_t *offsets, int32_t *perm, int32_t *inv_perm,
+                             void *workspace, size_t ws_bytes, moe_stream_t stream);
+
 /* Workspace bytes needed by moe_w4a16_forward (256-byte aligned buffer). */
 size_t moe_w4a16_workspace_size(int M, int k, int E, int H, int I);
 
@@ -159,6 +190,21 @@ moe_status_t moe_w4a16_forward(const uint16_t *hidden, const int32_t *topk_ids,
                                uint16_t *out, int M, int k, int E, int H, int I,
                                void *workspace, size_t ws_bytes,
                                moe_stream_t stream);
+
+/*
+ * moe_w4a16_forward from router logits: the router front-end of
+ * moe_route_align writes topk_ids [M][k] and topk_w [M][k] (caller-owned,
+ * device, 4-byte aligned) from logits [M][E] fp32, then the layer runs on
+ * them.  Other arguments, limits and the workspace are those of
+ * moe_w4a16_forward (same moe_w4a16_workspace_size), plus k <= E.  Bad
+ * logits are reported as in moe_route_align; their tokens' output rows are
+ * zero.
+ */
+moe_status_t moe_w4a16_forward_routed(const uint16_t *hidden, const float *logits,
+                                      const void *w13, const void *w2, uint16_t *out,
+                                      int32_t *topk_ids, float *topk_w, int M, int k,
+                                      int E, int H, int I, void *workspace,
+                                      size_t ws_bytes, moe_stream_t stream);
 
 /*
  * Same as moe_w4a16_forward, and additionally records CUDA events around each

@@ -28,6 +28,7 @@ MOE_ERR_CUDA = 6
 MOE_ERR_DEVICE_BAD_EXPERT_ID = 7
 MOE_ERR_DEVICE_TIMEOUT = 8
 MOE_ERR_DEVICE_FP16_RANGE = 9
+MOE_ERR_DEVICE_BAD_LOGIT = 10
 MOE_PACK_W13 = 1
 MOE_PACK_W2 = 2
 
@@ -71,7 +72,9 @@ def load(path: str = LIB_PATH):
             "moe_w4a16_prepack": (i, [i, p, p, i, i, i, i, p, sz, p]),
             "moe_align_workspace_size": (sz, [i, i, i]),
             "moe_align": (i, [p, i, i, i, p, p, p, p, p, sz, p]),
+            "moe_route_align": (i, [p, i, i, i, p, p, p, p, p, p, p, sz, p]),
             "moe_w4a16_workspace_size": (sz, [i, i, i, i, i]),
+            "moe_w4a16_forward_routed": (i, [p, p, p, p, p, p, p, i, i, i, i, i, p, sz, p]),
             "moe_w4a16_forward": (i, [p, p, p, p, p, p, i, i, i, i, i, p, sz, p]),
             "moe_w4a16_forward_profiled": (i, [p, p, p, p, p, p, i, i, i, i, i, p, sz, p,
                                                ctypes.POINTER(p), i]),
@@ -128,8 +131,22 @@ def moe_align(topk_ids, M, k, E, counts, offsets, perm, inv_perm, workspace, str
                             _stream(stream))
 
 
+def moe_route_align(logits, M, k, E, topk_ids, topk_w, counts, offsets, perm, inv_perm,
+                    workspace, stream=None):
+    return load().moe_route_align(_p(logits), M, k, E, _p(topk_ids), _p(topk_w), _p(counts),
+                                  _p(offsets), _p(perm), _p(inv_perm), _p(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
+
+
 def moe_w4a16_workspace_size(M, k, E, H, I):
     return load().moe_w4a16_workspace_size(M, k, E, H, I)
+
+
+def moe_w4a16_forward_routed(hidden, logits, w13, w2, out, topk_ids, topk_w, M, k, E, H, I,
+                             workspace, stream=None):
+    return load().moe_w4a16_forward_routed(
+        _p(hidden), _p(logits), _p(w13), _p(w2), _p(out), _p(topk_ids), _p(topk_w), M, k, E, H,
+        I, _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
 
 
 def moe_w4a16_forward(hidden, topk_ids, topk_w, w13, w2, out, M, k, E, H, I, workspace,
@@ -255,6 +272,24 @@ def align(topk_ids, E, stream=None):
     return counts, offsets, perm[:M * k], inv_perm[:M * k], ws
 
 
+def route_align(logits, k, stream=None):
+    """Router front-end + alignment from fp32 logits [M][E].  Returns
+    (topk_ids, topk_w, counts, offsets, perm, inv_perm, workspace)."""
+    import torch
+    M, E = logits.shape
+    dev = logits.device
+    ids = torch.empty((M, k), dtype=torch.int32, device=dev)
+    w = torch.empty((M, k), dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(max(M * k, 1), dtype=torch.int32, device=dev)
+    inv_perm = torch.empty(max(M * k, 1), dtype=torch.int32, device=dev)
+    ws = _empty_bytes(moe_align_workspace_size(M, k, E), dev)
+    _check(moe_route_align(logits.contiguous(), M, k, E, ids, w, counts, offsets, perm, inv_perm,
+                           ws, stream), "moe_route_align")
+    return ids, w, counts, offsets, perm[:M * k], inv_perm[:M * k], ws
+
+
 class Workspace:
     """A reusable forward workspace sized for up to ``max_M`` tokens."""
 
@@ -278,3 +313,21 @@ def forward(hidden, topk_ids, topk_w, w13, w2, E, I, out=None, workspace=None, s
     _check(moe_w4a16_forward(hidden, topk_ids, topk_w, w13, w2, out, M, k, E, H, I, ws, stream),
            "moe_w4a16_forward")
     return out
+
+
+def forward_routed(hidden, logits, k, w13, w2, E, I, out=None, workspace=None, stream=None):
+    """The layer from router logits [M][E] fp32: returns (out [M][H] bf16,
+    topk_ids [M][k], topk_w [M][k]); raises MoeError on a host-side error."""
+    import torch
+    M, H = hidden.shape
+    dev = hidden.device
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    ids = torch.empty((M, k), dtype=torch.int32, device=dev)
+    w = torch.empty((M, k), dtype=torch.float32, device=dev)
+    ws = workspace.buf if isinstance(workspace, Workspace) else workspace
+    if ws is None:
+        ws = Workspace(M, k, E, H, I, dev).buf
+    _check(moe_w4a16_forward_routed(hidden, logits.contiguous(), w13, w2, out, ids, w, M, k, E,
+                                    H, I, ws, stream), "moe_w4a16_forward_routed")
+    return out, ids, w

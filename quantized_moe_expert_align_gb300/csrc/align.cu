@@ -14,6 +14,7 @@
 // segment again in order, so the permutation is the stable counting sort by
 // expert of the flat index f = t*k + j.
 #include "device_common.cuh"
+#include "route.cuh"
 
 namespace moe {
 namespace {
@@ -59,13 +60,29 @@ __global__ void __launch_bounds__(kThreads, 1) align_kernel(AlignArgs a) {
     const int E = a.E, n = a.n;
 
     if (tid == 0) {
-        a.ctrl->status = 0;
-        a.ctrl->detail = 0;
+        if (a.reset_status) {
+            a.ctrl->status = 0;
+            a.ctrl->detail = 0;
+        }
         s_invalid = 0;
     }
     for (int i = tid; i < kWarps * E; i += kThreads) table[i] = 0;
     __syncthreads();
     pdl_trigger();
+
+    // Optional router front-end: warp w routes tokens w, w + 32, ...; the ids
+    // it writes are read back below by other warps of this CTA, after the
+    // barrier, with ordinary (coherent) loads.
+    if (a.logits) {
+        const int vpl = route_vpl(E);
+        for (int t = w; t < a.route_M; t += kWarps) {
+            const bool bad = route_row_any<kAlignRouteMaxVpl>(vpl, a.logits + (size_t)t * E, E, a.route_k, lane,
+                                           a.route_ids + (size_t)t * a.route_k,
+                                           a.route_w + (size_t)t * a.route_k);
+            if (bad && lane == 0) set_status(a.ctrl, MOE_ERR_DEVICE_BAD_LOGIT, t);
+        }
+        __syncthreads();
+    }
 
     const int per = (n + kWarps - 1) / kWarps;
     const int seg_lo = min(n, w * per), seg_hi = min(n, seg_lo + per);
@@ -77,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1) align_kernel(AlignArgs a) {
         const int f = base + lane;
         int id = -1;
         if (f < seg_hi) {
-            id = __ldg(a.ids + f);
+            id = a.ids[f];
             if (id < 0 || id >= E) {
                 if (my_invalid == 0) first_bad = id;
                 ++my_invalid;
@@ -138,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1) align_kernel(AlignArgs a) {
         const int f = base + lane;
         int id = -1;
         if (f < seg_hi) {
-            id = __ldg(a.ids + f);
+            id = a.ids[f];
             if (id < 0 || id >= E) id = -1;
         }
         const unsigned peers = __match_any_sync(0xffffffffu, id);

@@ -6,6 +6,7 @@
 
 #include "gemm_tc.h"
 #include "moe_internal.h"
+#include "route.cuh"
 
 namespace moe {
 
@@ -111,6 +112,29 @@ bool routing_sizes_ok(int M, int k, int E) {
     return M >= 0 && k >= 1 && k <= 64 && E >= 1 && E <= 1024 && (int64_t)M * k < INT_MAX;
 }
 
+// Routing ahead of the alignment kernel `a` (whose ids must be topk_ids):
+// small batches are routed by the alignment kernel itself, larger ones by
+// route_kernel first, after clearing the status word that the alignment
+// kernel then leaves alone.
+cudaError_t route_into(AlignArgs &a, const float *logits, int M, int k, int32_t *topk_ids,
+                       float *topk_w, cudaStream_t s) {
+    if (M <= kFusedRouteMaxM && route_vpl(a.E) <= kAlignRouteMaxVpl) {
+        a.logits = logits;
+        a.route_M = M;
+        a.route_k = k;
+        a.route_ids = topk_ids;
+        a.route_w = topk_w;
+        a.reset_status = 1;
+        return cudaSuccess;
+    }
+    a.logits = nullptr;
+    a.reset_status = 0;
+    cudaError_t err = cudaMemsetAsync(a.ctrl, 0, 2 * sizeof(int32_t), s);
+    if (err != cudaSuccess) return err;
+    RouteArgs r = {logits, M, a.E, k, topk_ids, topk_w, a.ctrl};
+    return launch_route(r, s);
+}
+
 bool layer_sizes_ok(int M, int k, int E, int H, int I) {
     return routing_sizes_ok(M, k, E) && H > 0 && I > 0 && H % kChunkK == 0 &&
            I % kChunkK == 0 && H <= (1 << 20) && I <= (1 << 20) &&
@@ -136,6 +160,7 @@ const char *moe_status_string(moe_status_t s) {
         case MOE_ERR_DEVICE_BAD_EXPERT_ID: return "MOE_ERR_DEVICE_BAD_EXPERT_ID: expert id outside [0, E)";
         case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
         case MOE_ERR_DEVICE_FP16_RANGE: return "MOE_ERR_DEVICE_FP16_RANGE: value not representable in fp16";
+        case MOE_ERR_DEVICE_BAD_LOGIT: return "MOE_ERR_DEVICE_BAD_LOGIT: a router logit is NaN or +inf";
     }
     return "MOE_ERR_UNKNOWN";
 }
@@ -214,6 +239,7 @@ moe_status_t moe_align(const int32_t *ids, int M, int k, int E, int32_t *counts,
     a.ids = ids;
     a.n = M * k;
     a.E = E;
+    a.reset_status = 1;
     a.token_tile = 0;
     a.counts = counts;
     a.offsets = offsets;
@@ -228,20 +254,60 @@ moe_status_t moe_align(const int32_t *ids, int M, int k, int E, int32_t *counts,
     return MOE_OK;
 }
 
+moe_status_t moe_route_align(const float *logits, int M, int k, int E, int32_t *topk_ids,
+                             float *topk_w, int32_t *counts, int32_t *offsets, int32_t *perm,
+                             int32_t *inv_perm, void *workspace, size_t ws_bytes,
+                             moe_stream_t stream) {
+    if (!routing_sizes_ok(M, k, E) || k > E) return MOE_ERR_INVALID_ARG;
+    if (!counts || !offsets || !workspace ||
+        (M > 0 && (!logits || !topk_ids || !topk_w || !perm)))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) ||
+        !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(perm, 4) ||
+        !aligned(inv_perm, 4) || !aligned(workspace, 256))
+        return MOE_ERR_MISALIGNED;
+    if (ws_bytes < align_layout(M, k, E).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    moe_status_t st = check_device();
+    if (st != MOE_OK) return st;
+    Ctrl *ctrl =
+        reinterpret_cast<Ctrl *>(static_cast<uint8_t *>(workspace) + align_layout(M, k, E).ctrl);
+    AlignArgs a = {};
+    a.ids = topk_ids;
+    a.n = M * k;
+    a.E = E;
+    a.counts = counts;
+    a.offsets = offsets;
+    a.perm = perm;
+    a.inv_perm = inv_perm;
+    a.ctrl = ctrl;
+    if (route_into(a, logits, M, k, topk_ids, topk_w, reinterpret_cast<cudaStream_t>(stream)) !=
+            cudaSuccess ||
+        launch_align(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
 size_t moe_w4a16_workspace_size(int M, int k, int E, int H, int I) {
     if (!layer_sizes_ok(M, k, E, H, I)) return 0;
     return fwd_layout(M, k, E, H, I).total;
 }
 
+// The forward; with `logits` non-null the router front-end first writes ids
+// and topk_w (then caller-owned outputs) from the logits.
 static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, const float *topk_w,
                                  const void *w13, const void *w2, uint16_t *out, int M, int k,
                                  int E, int H, int I, void *workspace, size_t ws_bytes,
-                                 moe_stream_t stream, cudaEvent_t *ev) {
+                                 moe_stream_t stream, cudaEvent_t *ev,
+                                 const float *logits = nullptr) {
     if (!layer_sizes_ok(M, k, E, H, I)) return MOE_ERR_INVALID_ARG;
+    if (logits && k > E) return MOE_ERR_INVALID_ARG;
     if (!w13 || !w2 || !workspace) return MOE_ERR_INVALID_ARG;
     if (M > 0 && (!hidden || !ids || !topk_w || !out)) return MOE_ERR_INVALID_ARG;
     if (!aligned(hidden, 16) || !aligned(out, 16) || !aligned(ids, 4) || !aligned(topk_w, 4) ||
-        !aligned(w13, 256) || !aligned(w2, 256) || !aligned(workspace, 256))
+        !aligned(logits, 4) || !aligned(w13, 256) || !aligned(w2, 256) ||
+        !aligned(workspace, 256))
         return MOE_ERR_MISALIGNED;
     const FwdLayout L = fwd_layout(M, k, E, H, I);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -275,8 +341,24 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     const int n = M * k;
     const int r1 = 4 * (2 * I / kTileRows), r2 = 4 * (H / kTileRows);  // tickets per token tile
 
-    AlignArgs al = {ids, n, E, L.nt, L.nt2, counts, offsets, perm, inv_perm, tile_prefix,
-                    tile_prefix2, ctrl, tickets, r1, r2, L.max_tok_tiles * r1};
+    AlignArgs al = {};
+    al.ids = ids;
+    al.n = n;
+    al.E = E;
+    al.reset_status = 1;
+    al.token_tile = L.nt;
+    al.token_tile2 = L.nt2;
+    al.counts = counts;
+    al.offsets = offsets;
+    al.perm = perm;
+    al.inv_perm = inv_perm;
+    al.tile_prefix = tile_prefix;
+    al.tile_prefix2 = tile_prefix2;
+    al.ctrl = ctrl;
+    al.tickets = tickets;
+    al.r1 = r1;
+    al.r2 = r2;
+    al.off2 = L.max_tok_tiles * r1;
     GatherArgs ga = {hidden, perm, offsets, n, k, H, E, xs, ctrl};
     TcArgs g1 = {};
     g1.w = static_cast<const uint8_t *>(w13);
@@ -311,6 +393,14 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
 
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
     const bool pdl = (ev == nullptr);
+    const bool route_kernel =
+        logits && (M > kFusedRouteMaxM || route_vpl(E) > kAlignRouteMaxVpl);
+    if (logits &&
+        route_into(al, logits, M, k, const_cast<int32_t *>(ids), const_cast<float *>(topk_w), s) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
     if (mark(0) != cudaSuccess || launch_align(al, s) != cudaSuccess || mark(1) != cudaSuccess ||
         launch_gather_hidden(ga, s, pdl) != cudaSuccess || mark(2) != cudaSuccess ||
         launch_gemm_tc(g1, map_x, grid, s, pdl) != cudaSuccess || mark(3) != cudaSuccess ||
@@ -327,7 +417,7 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     g_diag.token_tile = L.nt;
     g_diag.grid_gemm1 = grid;
     g_diag.grid_gemm2 = grid;
-    g_diag.kernels_launched = 5;
+    g_diag.kernels_launched = route_kernel ? 6 : 5;
     g_diag.workspace_bytes = (int64_t)L.total;
     g_diag.calls += 1;
     return MOE_OK;
@@ -339,6 +429,16 @@ moe_status_t moe_w4a16_forward(const uint16_t *hidden, const int32_t *ids, const
                                size_t ws_bytes, moe_stream_t stream) {
     return forward_impl(hidden, ids, topk_w, w13, w2, out, M, k, E, H, I, workspace,
                         ws_bytes, stream, nullptr);
+}
+
+moe_status_t moe_w4a16_forward_routed(const uint16_t *hidden, const float *logits,
+                                      const void *w13, const void *w2, uint16_t *out,
+                                      int32_t *topk_ids, float *topk_w, int M, int k, int E,
+                                      int H, int I, void *workspace, size_t ws_bytes,
+                                      moe_stream_t stream) {
+    if (M > 0 && !logits) return MOE_ERR_INVALID_ARG;
+    return forward_impl(hidden, topk_ids, topk_w, w13, w2, out, M, k, E, H, I, workspace,
+                        ws_bytes, stream, nullptr, M > 0 ? logits : nullptr);
 }
 
 moe_status_t moe_w4a16_forward_profiled(const uint16_t *hidden, const int32_t *ids,

@@ -113,6 +113,14 @@ struct AlignArgs {
     const int32_t *ids;
     int n;            // M * k
     int E;
+    int reset_status; // nonzero: this kernel starts the call (clears the status word)
+    // Routing inside the alignment kernel (logits non-null): the kernel first
+    // writes route_ids / route_w for route_M tokens of route_k slots from
+    // logits [route_M][E], then aligns route_ids (ids must equal route_ids).
+    const float *logits;
+    int route_M, route_k;
+    int32_t *route_ids;
+    float *route_w;
     int token_tile;   // >0: also write tile_prefix for this tile width,
     int token_tile2;  //     and tile_prefix2 for this one
     int32_t *counts, *offsets, *perm, *inv_perm, *tile_prefix, *tile_prefix2;
@@ -121,6 +129,19 @@ struct AlignArgs {
     int r1, r2, off2;
 };
 cudaError_t launch_align(const AlignArgs &a, cudaStream_t s);
+
+// Router front-end: topk ids / weights from fp32 logits, one warp per token.
+struct RouteArgs {
+    const float *logits;  // [M][E]
+    int M, E, k;
+    int32_t *ids;         // [M][k]
+    float *w;             // [M][k]
+    Ctrl *ctrl;
+};
+cudaError_t launch_route(const RouteArgs &a, cudaStream_t s);
+// Batches up to this many tokens are routed inside the alignment kernel
+// (32 warps, at most two tokens each); larger ones by route_kernel first.
+constexpr int kFusedRouteMaxM = 64;
 
 // Both write into the blocks after the header of a prepacked buffer `dst`.
 cudaError_t launch_prepack_codes(int kind, const uint8_t *q, int E, int N, int K,

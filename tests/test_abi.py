@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(10):
+    for code in range(11):
         s = moe.moe_status_string(code)
         assert s.startswith("MOE_")
     assert moe.moe_status_string(0) == "MOE_OK"
@@ -111,6 +111,36 @@ def test_align_and_prepack_host_validation(lib):
         moe.MOE_ERR_MISALIGNED
     assert lib.moe_w4a16_prepack(1, None, p, 8, 256, 256, 32, p, 1 << 30, None) == \
         moe.MOE_ERR_INVALID_ARG
+
+
+def test_router_host_validation(lib):
+    p = 4096
+    ra = lib.moe_route_align
+    args = [p, 4, 2, 8, p, p, p, p, p, p, p, 1 << 20, None]
+
+    def call(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return ra(*a)
+    assert call(a3=1) == moe.MOE_ERR_INVALID_ARG           # k > E
+    assert call(a2=0) == moe.MOE_ERR_INVALID_ARG           # k = 0
+    assert call(a0=None) == moe.MOE_ERR_INVALID_ARG        # logits
+    assert call(a5=None) == moe.MOE_ERR_INVALID_ARG        # topk_w
+    assert call(a0=p + 2) == moe.MOE_ERR_MISALIGNED
+    assert call(a10=p + 64) == moe.MOE_ERR_MISALIGNED      # workspace
+    assert call(a11=16) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+    fr = lib.moe_w4a16_forward_routed
+    good = [p, p, p, p, p, p, p, 4, 2, 8, 256, 128, p, 1 << 30, None]
+    bad = list(good)
+    bad[1] = None
+    assert fr(*bad) == moe.MOE_ERR_INVALID_ARG             # logits
+    bad = list(good)
+    bad[8], bad[9] = 9, 8
+    assert fr(*bad) == moe.MOE_ERR_INVALID_ARG             # k > E
+    bad = list(good)
+    bad[1] = p + 1
+    assert fr(*bad) == moe.MOE_ERR_MISALIGNED
 
 
 def test_no_gpu_reports_unsupported_device(lib):
