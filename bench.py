@@ -341,8 +341,12 @@ def our_arm(args, wl):
 
     # ---- router front-end: logits -> ids, weights and alignment alone
     # (moe_route_align), and the whole layer from logits
-    # (moe_w4a16_forward_routed); same logits as the batches' routing ----
+    # (moe_w4a16_forward_routed, L2 flushed before each call as in the timed
+    # steps); same logits as the batches' routing.  A device-side sleep first
+    # lets the host queue the calls ahead of the GPU, so that the events time
+    # the kernels, not the host's launch latency.
     router = {}
+    reps = max(5, min(args.steps, 20))
     for M in wl.Ms:
         x, ids, w, out = devb[M]
         lg = dev(synth.logits(M, L.E, seed=0, zipf_s=wl.zipf_s))
@@ -354,21 +358,35 @@ def our_arm(args, wl):
         inv = torch.empty(M * L.k, dtype=torch.int32, device="cuda")
         aws = torch.empty(max(moe.moe_align_workspace_size(M, L.k, L.E), 256),
                           dtype=torch.uint8, device="cuda")
-        t_route = t_layer = 0.0
-        for _ in range(prof_steps):
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-            flush.zero_()
-            evs[0].record(stream)
+
+        def route_call():
             st = moe.moe_route_align(lg, M, L.k, L.E, r_ids, r_w, cnt, off, perm, inv, aws, stream)
-            evs[1].record(stream)
-            st2 = moe.moe_w4a16_forward_routed(x, lg, p13, p2, out, r_ids, r_w, M, L.k, L.E,
-                                               L.H, L.I, ws.buf, stream)
-            evs[2].record(stream)
-            if st != moe.MOE_OK or st2 != moe.MOE_OK:
-                raise moe.MoeError(st or st2, "router front-end")
-            torch.cuda.synchronize()
-            t_route += evs[0].elapsed_time(evs[1]) / prof_steps
-            t_layer += evs[1].elapsed_time(evs[2]) / prof_steps
+            if st != moe.MOE_OK:
+                raise moe.MoeError(st, "moe_route_align")
+
+        def layer_call():
+            st = moe.moe_w4a16_forward_routed(x, lg, p13, p2, out, r_ids, r_w, M, L.k, L.E,
+                                              L.H, L.I, ws.buf, stream)
+            if st != moe.MOE_OK:
+                raise moe.MoeError(st, "moe_w4a16_forward_routed")
+
+        route_call()
+        layer_call()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 + 2 * reps)]
+        torch.cuda._sleep(4_000_000)
+        ev[0].record(stream)
+        for _ in range(reps):
+            route_call()
+        ev[1].record(stream)
+        for r in range(reps):
+            flush.zero_()
+            ev[2 + 2 * r].record(stream)
+            layer_call()
+            ev[3 + 2 * r].record(stream)
+        torch.cuda.synchronize()
+        t_route = ev[0].elapsed_time(ev[1]) / reps
+        t_layer = float(np.mean([ev[2 + 2 * r].elapsed_time(ev[3 + 2 * r]) for r in range(reps)]))
         st, detail = moe.moe_w4a16_get_device_status(ws.buf)
         if st != moe.MOE_OK:
             raise moe.MoeError(st, f"routed forward device status (detail {detail})")
@@ -376,6 +394,7 @@ def our_arm(args, wl):
             raise RuntimeError(f"routed ids differ from the batch's routing at M={M}")
         nbytes = M * L.E * 4 + M * L.k * 8
         router[M] = {"route_align_us": round(1e3 * t_route, 2),
+                     "route_align_timing": f"mean of {reps} back-to-back calls, warm L2",
                      "route_bytes": nbytes,
                      "route_gbs": round(nbytes / (t_route / 1e3) / 1e9, 1),
                      "us_per_call_from_logits": round(1e3 * t_layer, 2)}
