@@ -61,14 +61,14 @@ class Oracle:
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_dequant_element.restype = ctypes.c_double
-        lib.oracle_dequant_element.argtypes = [p, p, i64, i64, i64]
+        lib.oracle_dequant_element.argtypes = [p, p, i64, i64, i64, i64]
         lib.oracle_align.restype = i64
         lib.oracle_align.argtypes = [p, i64, i64, i64, p, p, p, p]
         lib.oracle_route.restype = i64
         lib.oracle_route.argtypes = [p, i64, i64, i64, p, p]
         lib.oracle_forward.restype = i64
         lib.oracle_forward.argtypes = [p, p, p, p, p, p, p,
-                                       i64, i64, i64, i64, i64,
+                                       i64, i64, i64, i64, i64, i64,
                                        p, p, p, p, p, p, p, p, i64]
         self.lib = lib
         self.path = so_path
@@ -77,11 +77,14 @@ class Oracle:
         return int(self.lib.oracle_num_threads())
 
     def dequant_element(self, q, s, n: int, kk: int) -> float:
-        """Dequantised element (n, kk) of one packed [N][K/2] matrix."""
+        """Dequantised element (n, kk) of one packed [N][K/2] matrix with
+        [N][K/group] scales (the group size follows from the shapes)."""
         q = np.ascontiguousarray(q, dtype=np.uint8)
         s = np.ascontiguousarray(s, dtype=np.uint16)
         K = q.shape[1] * 2
-        return float(self.lib.oracle_dequant_element(_ptr(q), _ptr(s), K, n, kk))
+        group = K // s.shape[1]
+        assert group * s.shape[1] == K
+        return float(self.lib.oracle_dequant_element(_ptr(q), _ptr(s), K, group, n, kk))
 
     def align(self, ids, E: int):
         """Stable counting sort of the flat slot indices by expert.
@@ -119,6 +122,9 @@ class Oracle:
         """Layer forward in double.  ``hidden`` and the scales are bf16 bit
         patterns (uint16); packed weights are canonical [E][N][K/2] bytes.
 
+        The scale group size (32 on the pages; 64 and 128 also work) follows
+        from the scale shapes [E][N][K/group].
+
         Returns ``out`` [M][H] float64, or with ``want_intermediates`` a dict
         with ``out``, ``act`` ([M*k][I], sorted order), ``y`` ([M*k][H],
         sorted order) and the alignment.
@@ -128,8 +134,10 @@ class Oracle:
         topk_w = np.ascontiguousarray(topk_w, dtype=np.float32)
         M, k = ids.shape
         assert hidden.shape == (M, H) and topk_w.shape == (M, k)
-        assert w13.shape == (E, 2 * I, H // 2) and s13.shape == (E, 2 * I, H // 32)
-        assert w2.shape == (E, H, I // 2) and s2.shape == (E, H, I // 32)
+        group = H // s13.shape[2]
+        assert group * s13.shape[2] == H and I % group == 0
+        assert w13.shape == (E, 2 * I, H // 2) and s13.shape == (E, 2 * I, H // group)
+        assert w2.shape == (E, H, I // 2) and s2.shape == (E, H, I // group)
         assert w13.dtype == np.uint8 and w2.dtype == np.uint8
         assert s13.dtype == np.uint16 and s2.dtype == np.uint16
         n = M * k
@@ -144,7 +152,7 @@ class Oracle:
         inv_perm = np.full(max(n, 1), -1, np.int32)
         bad = self.lib.oracle_forward(
             _ptr(hidden), _ptr(ids), _ptr(topk_w), _ptr(w13), _ptr(s13), _ptr(w2),
-            _ptr(s2), M, k, E, H, I, _ptr(out), _ptr(act), _ptr(y), _ptr(counts),
+            _ptr(s2), M, k, E, H, I, group, _ptr(out), _ptr(act), _ptr(y), _ptr(counts),
             _ptr(offsets), _ptr(perm), _ptr(inv_perm), _ptr(scratch), nt * I)
         if bad < 0:
             raise RuntimeError("oracle_forward: scratch too small")

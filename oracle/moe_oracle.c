@@ -29,7 +29,8 @@
  * The pages print no formula.  The readings used here (each one is also
  * listed in the design notes):
  *  - dequantised weight = (q - 8) * scale, q in [0, 15], one bf16 scale per
- *    group of 32 consecutive elements along K (the reduction axis);
+ *    group of consecutive elements along K (the reduction axis): 32 as on
+ *    the pages, or 64 / 128 for the wider-group variant;
  *  - canonical packing: byte kk/2 of a row holds element kk in its low nibble
  *    when kk is even and in its high nibble when kk is odd;
  *  - w13 rows [0, I) are the gate projection, rows [I, 2I) the up projection;
@@ -73,12 +74,12 @@ static int code_at(const uint8_t *q, int64_t K, int64_t n, int64_t kk)
     return (kk & 1) ? (byte >> 4) : (byte & 0x0F);
 }
 
-/* Dequantised weight W[n][kk] = (q - 8) * scale[n][kk / 32]. */
+/* Dequantised weight W[n][kk] = (q - 8) * scale[n][kk / group]. */
 static double weight_at(const uint8_t *q, const uint16_t *s, int64_t K,
-                        int64_t n, int64_t kk)
+                        int64_t group, int64_t n, int64_t kk)
 {
     int code = code_at(q, K, n, kk);
-    double scale = bf16_to_double(s[n * (K / 32) + kk / 32]);
+    double scale = bf16_to_double(s[n * (K / group) + kk / group]);
     return (double)(code - 8) * scale;
 }
 
@@ -94,11 +95,11 @@ int oracle_num_threads(void)
 }
 
 /* Exposed for the byte-level pins: dequantised value of element (n, kk) of
- * a single [N][K/2] packed matrix with [N][K/32] bf16 scales. */
+ * a single [N][K/2] packed matrix with [N][K/group] bf16 scales. */
 double oracle_dequant_element(const uint8_t *q, const uint16_t *s, int64_t K,
-                              int64_t n, int64_t kk)
+                              int64_t group, int64_t n, int64_t kk)
 {
-    return weight_at(q, s, K, n, kk);
+    return weight_at(q, s, K, group, n, kk);
 }
 
 /*
@@ -155,6 +156,7 @@ int64_t oracle_forward(const uint16_t *hidden, const int32_t *ids,
                        const uint8_t *w13, const uint16_t *s13,
                        const uint8_t *w2, const uint16_t *s2,
                        int64_t M, int64_t k, int64_t E, int64_t H, int64_t I,
+                       int64_t group,
                        double *out, double *act, double *yrow,
                        int32_t *counts, int32_t *offsets, int32_t *perm,
                        int32_t *inv_perm, double *a_scratch,
@@ -162,8 +164,8 @@ int64_t oracle_forward(const uint16_t *hidden, const int32_t *ids,
 {
     int64_t invalid = oracle_align(ids, M, k, E, counts, offsets, perm, inv_perm);
     int64_t n_valid = offsets[E];
-    const int64_t w13_expert = 2 * I * (H / 2), s13_expert = 2 * I * (H / 32);
-    const int64_t w2_expert = H * (I / 2), s2_expert = H * (I / 32);
+    const int64_t w13_expert = 2 * I * (H / 2), s13_expert = 2 * I * (H / group);
+    const int64_t w2_expert = H * (I / 2), s2_expert = H * (I / group);
     if (!act && a_scratch_len < (int64_t)oracle_num_threads() * I) return -1;
 
     /* Grouped stages: each sorted position p is one (token, slot) row of its
@@ -189,8 +191,8 @@ int64_t oracle_forward(const uint16_t *hidden, const int32_t *ids,
             double g = 0.0, u = 0.0;
             for (int64_t h = 0; h < H; ++h) {
                 double xv = bf16_to_double(x[h]);
-                g += xv * weight_at(q13, sc13, H, n, h);
-                u += xv * weight_at(q13, sc13, H, I + n, h);
+                g += xv * weight_at(q13, sc13, H, group, n, h);
+                u += xv * weight_at(q13, sc13, H, group, I + n, h);
             }
             a[n] = silu(g) * u;
         }
@@ -199,7 +201,7 @@ int64_t oracle_forward(const uint16_t *hidden, const int32_t *ids,
         for (int64_t hh = 0; hh < H; ++hh) {
             double acc = 0.0;
             for (int64_t n = 0; n < I; ++n)
-                acc += a[n] * weight_at(q2, sc2, I, hh, n);
+                acc += a[n] * weight_at(q2, sc2, I, group, hh, n);
             y[hh] = acc;
         }
     }

@@ -8,7 +8,8 @@ oracle with planted mistakes and requires every mistake to be caught.
 
 What each pin rests on:
   * worked bytes  -- the packed-code convention and the dequantisation rule
-    (value = (q - 8) * scale, group of 32 along K), evaluated by hand;
+    (value = (q - 8) * scale, group of 32 along K; 64 and 128 for the
+    wider-group variant), evaluated by hand;
   * stable sort   -- the alignment is a stable counting sort, so it must equal
     numpy's stable argsort and bincount/cumsum;
   * closed form   -- weights whose codes are constant along K make every
@@ -45,12 +46,14 @@ def _bf16(b):
 
 
 def dense_weight(q: np.ndarray, s: np.ndarray) -> np.ndarray:
-    """Unpack one canonical [N][K/2] code matrix into a dense fp64 [N][K]."""
+    """Unpack one canonical [N][K/2] code matrix with [N][K/group] scales into
+    a dense fp64 [N][K]."""
     N, half = q.shape
     codes = np.empty((N, 2 * half), np.int64)
     codes[:, 0::2] = q & 0x0F
     codes[:, 1::2] = q >> 4
-    return (codes - 8).astype(np.float64) * np.repeat(_bf16(s), 32, axis=1)
+    group = 2 * half // s.shape[1]
+    return (codes - 8).astype(np.float64) * np.repeat(_bf16(s), group, axis=1)
 
 
 def brute_force(hidden, ids, topk_w, w13, s13, w2, s2, E, H, I):
@@ -74,11 +77,12 @@ def brute_force(hidden, ids, topk_w, w13, s13, w2, s2, E, H, I):
     return out
 
 
-def _random_layer(rng, E, H, I):
+def _random_layer(rng, E, H, I, group=32):
     w13 = rng.integers(0, 256, size=(E, 2 * I, H // 2), dtype=np.uint8)
     w2 = rng.integers(0, 256, size=(E, H, I // 2), dtype=np.uint8)
-    s13 = synth.f32_to_bf16_bits(rng.uniform(0.002, 0.02, (E, 2 * I, H // 32)).astype(np.float32))
-    s2 = synth.f32_to_bf16_bits(rng.uniform(0.002, 0.02, (E, H, I // 32)).astype(np.float32))
+    s13 = synth.f32_to_bf16_bits(
+        rng.uniform(0.002, 0.02, (E, 2 * I, H // group)).astype(np.float32))
+    s2 = synth.f32_to_bf16_bits(rng.uniform(0.002, 0.02, (E, H, I // group)).astype(np.float32))
     return w13, s13, w2, s2
 
 
@@ -194,6 +198,38 @@ def check_forward_closed_form(orc):
             y = sd * (d[e].astype(np.float64) @ a)
             ref += float(w[t, j]) * y
         _close(out[t], ref, 1e-9)
+
+
+def check_dequant_wide_groups(orc):
+    """Hand-evaluated scale indexing for groups of 64 and 128: element kk
+    takes scale kk // group."""
+    K = 256
+    q = np.full((1, K // 2), 0x88, np.uint8)
+    q[0, 31] = 0xA8      # element 63 -> code 10, element 62 -> 8
+    q[0, 32] = 0x89      # element 64 -> code 9
+    q[0, 63] = 0xB8      # element 127 -> code 11
+    q[0, 64] = 0x8F      # element 128 -> code 15
+    q[0, 127] = 0x08     # element 255 -> code 0
+    s64 = np.array([[BF16_ONE_QUARTER, BF16_THREE, BF16_ONE_QUARTER, BF16_THREE]], np.uint16)
+    expect64 = {63: 2 * 0.25, 64: 1 * 3.0, 127: 3 * 3.0, 128: 7 * 0.25, 255: -8 * 3.0, 62: 0.0}
+    for kk, v in expect64.items():
+        got = orc.dequant_element(q, s64, 0, kk)
+        assert got == v, f"group 64, element {kk}: {got} != {v}"
+    s128 = np.array([[BF16_THREE, BF16_ONE_QUARTER]], np.uint16)
+    expect128 = {63: 2 * 3.0, 64: 1 * 3.0, 127: 3 * 3.0, 128: 7 * 0.25, 255: -8 * 0.25}
+    for kk, v in expect128.items():
+        got = orc.dequant_element(q, s128, 0, kk)
+        assert got == v, f"group 128, element {kk}: {got} != {v}"
+
+
+def check_forward_brute_force_wide_groups(orc):
+    rng = np.random.default_rng(31)
+    for group in (64, 128):
+        for (M, E, H, I, k) in [(4, 6, 256, 128, 2), (3, 3, 128, 128, 3)]:
+            w13, s13, w2, s2 = _random_layer(rng, E, H, I, group)
+            hidden, ids, w = _random_inputs(rng, M, E, H, k)
+            out = orc.forward(hidden, ids, w, w13, s13, w2, s2, E, H, I)
+            _close(out, brute_force(hidden, ids, w, w13, s13, w2, s2, E, H, I))
 
 
 def check_forward_brute_force(orc):
@@ -387,7 +423,8 @@ def check_route_matches_input_generator(orc):
         assert np.all(np.abs(w - w_ref) <= 2.0 ** -23 * w_ref)
 
 
-ALL_PINS = [check_route_selection_brute_force, check_route_weights_full_softmax,
+ALL_PINS = [check_dequant_wide_groups, check_forward_brute_force_wide_groups,
+            check_route_selection_brute_force, check_route_weights_full_softmax,
             check_route_closed_forms, check_route_special_values,
             check_route_matches_input_generator,
             check_dequant_worked_bytes, check_align_matches_stable_sort,

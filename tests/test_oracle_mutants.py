@@ -13,13 +13,14 @@ MUTANTS = [
     ("zero point 7", "(double)(code - 8)", "(double)(code - 7)"),
     ("nibble order swapped", "(kk & 1) ? (byte >> 4) : (byte & 0x0F)",
      "(kk & 1) ? (byte & 0x0F) : (byte >> 4)"),
-    ("first group scale only", "s[n * (K / 32) + kk / 32]", "s[n * (K / 32)]"),
+    ("first group scale only", "s[n * (K / group) + kk / group]", "s[n * (K / group)]"),
+    ("group size fixed at 32", "s[n * (K / group) + kk / group]", "s[n * (K / group) + kk / 32]"),
     ("silu sign", "exp(-v)", "exp(v)"),
     ("gate and up swapped", "a[n] = silu(g) * u;", "a[n] = silu(u) * g;"),
-    ("up rows interleaved", "weight_at(q13, sc13, H, I + n, h)",
-     "weight_at(q13, sc13, H, 2 * n + 1 < 2 * I ? 2 * n + 1 : n, h)"),
-    ("down projection transposed", "weight_at(q2, sc2, I, hh, n)",
-     "weight_at(q2, sc2, I, n, hh % I)"),
+    ("up rows interleaved", "weight_at(q13, sc13, H, group, I + n, h)",
+     "weight_at(q13, sc13, H, group, 2 * n + 1 < 2 * I ? 2 * n + 1 : n, h)"),
+    ("down projection transposed", "weight_at(q2, sc2, I, group, hh, n)",
+     "weight_at(q2, sc2, I, group, n, hh % I)"),
     ("first hidden element dropped", "for (int64_t h = 0; h < H; ++h)",
      "for (int64_t h = 1; h < H; ++h)"),
     ("combine ignores topk_w", "acc += (double)topk_w[t * k + j] * yrow",
