@@ -5,7 +5,8 @@ One step = one forward call per batch size of the workload (default: the
 decode sweep M in {1, 9, 90} of an E=384, H=7168, I=2048, top-8, INT4 g32
 layer), inputs already resident in HBM, L2 flushed before every step.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode|plateau|prefill|second|toy]
+  python bench.py [--gpus N] [--steps K] [--warmup W]
+                  [--config decode|plateau|prefill|second|toy|e256|group128]
                   [--impl ours|reference]
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the plain CPU
@@ -34,7 +35,8 @@ import synth  # noqa: E402
 
 METRIC = ("MoE layer µs/call & tokens/s vs M (1–16384); HBM GB/s or tensor-pipe % of peak")
 CONFIGS = {"decode": synth.DECODE, "plateau": synth.PLATEAU, "prefill": synth.PREFILL,
-           "second": synth.SECOND, "toy": synth.TOY}
+           "second": synth.SECOND, "toy": synth.TOY, "e256": synth.E256,
+           "group128": synth.GROUP128}
 # The pages' sweep on one RTX PRO 6000 (sm_120), context only: ms per call.
 PAGES_MS = {1: 0.151, 9: 1.18, 90: 5.19, 256: 7.02, 512: 7.01, 1024: 7.02}
 KERNELS = ["align", "gather", "gemm_gate_up", "gemm_down", "combine"]
@@ -73,8 +75,10 @@ def peaks():
 
 
 def expert_bytes(L):
-    w13 = 2 * L.I * L.H // 2 + 2 * L.I * (L.H // 32) * 2
-    w2 = L.H * L.I // 2 + L.H * (L.I // 32) * 2
+    """Algorithmic bytes of one expert's codes + bf16 scales (at the layer's
+    scale group), for w13 and w2."""
+    w13 = 2 * L.I * L.H // 2 + 2 * L.I * (L.H // L.group) * 2
+    w2 = L.H * L.I // 2 + L.H * (L.I // L.group) * 2
     return w13, w2
 
 
@@ -222,7 +226,7 @@ def reference_arm(args, wl):
         "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "Ms": list(wl.Ms), "E": L.E, "H": L.H, "I": L.I,
-                   "k": L.k, "group": 32, "parallelism": "none (host CPU)"},
+                   "k": L.k, "group": L.group, "parallelism": "none (host CPU)"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": describe_sample(sample, wl)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -482,7 +486,7 @@ def our_arm(args, wl):
             "vs_baseline": vs, "dtype": "f16 MMA operands, f32 accumulate (int4 weights)",
             "data": "synthetic",
             "config": {"workload": wl.name, "Ms": list(wl.Ms), "E": L.E, "H": L.H, "I": L.I,
-                       "k": L.k, "group": 32,
+                       "k": L.k, "group": L.group,
                        "routing": "zipf(1.1)-biased" if wl.zipf_s else "uniform",
                        "l2": "flushed before every step (write of 2x L2)",
                        "parallelism": f"replicas x{world}",

@@ -75,9 +75,9 @@ const char *moe_status_string(moe_status_t status);
 
 /*
  * Bytes of the prepacked buffer for one matrix: a 256-byte header, then
- * 9 KiB per (expert, 128-row tile, 128-element K chunk).  Requires
- * group == 32, N % 128 == 0, K % 128 == 0, E >= 1; otherwise returns
- * MOE_ERR_INVALID_ARG and sets *bytes to 0.
+ * 9 KiB per (expert, 128-row tile, 128-element K chunk), whatever the
+ * group.  Requires group in {32, 64, 128}, N % 128 == 0, K % 128 == 0,
+ * E >= 1; otherwise returns MOE_ERR_INVALID_ARG and sets *bytes to 0.
  */
 moe_status_t moe_w4a16_prepack_size(int kind, int E, int N, int K, int group,
                                     size_t *bytes);
@@ -90,7 +90,11 @@ moe_status_t moe_w4a16_prepack_size(int kind, int E, int N, int K, int group,
  *
  *  q_canon [E][N][K/2] uint8, device: element kk of row n sits in byte kk/2,
  *          in the low nibble when kk is even, the high nibble when odd.
- *  scales  [E][N][K/32] bf16 bit patterns, device.
+ *  scales  [E][N][K/group] bf16 bit patterns, device: one scale per `group`
+ *          consecutive elements of K.  The pages' layer uses group = 32;
+ *          64 and 128 (a variant this library adds) are stored in the same
+ *          packed layout, each scale repeated into the 32-element slots it
+ *          covers, so the forward is the same for all three.
  *  dst     device buffer of at least moe_w4a16_prepack_size bytes,
  *          256-byte aligned; the caller owns it.
  * Layout written: per expert, 128-row tiles (for w13 each tile holds 64 gate

@@ -241,18 +241,19 @@ def _empty_bytes(nbytes, device):
 
 
 def prepack(kind, q_canon, scales, stream=None):
-    """Prepack canonical codes [E][N][K/2] (uint8) and bf16 scales [E][N][K/32]
-    (int16/uint16/bfloat16 bits) that live on the GPU; returns the packed
-    uint8 buffer."""
+    """Prepack canonical codes [E][N][K/2] (uint8) and bf16 scales
+    [E][N][K/group] (int16/uint16/bfloat16 bits; group 32, 64 or 128, taken
+    from the shapes) that live on the GPU; returns the packed uint8 buffer."""
     import torch
     E, N, half = q_canon.shape
     K = half * 2
-    st, nb = moe_w4a16_prepack_size(kind, E, N, K, 32)
+    group = K // scales.shape[2]
+    st, nb = moe_w4a16_prepack_size(kind, E, N, K, group)
     _check(st, "moe_w4a16_prepack_size")
     packed = _empty_bytes(nb, q_canon.device)
     if scales.dtype == torch.bfloat16:
         scales = scales.view(torch.int16)
-    _check(moe_w4a16_prepack(kind, q_canon.contiguous(), scales.contiguous(), E, N, K, 32,
+    _check(moe_w4a16_prepack(kind, q_canon.contiguous(), scales.contiguous(), E, N, K, group,
                              packed, stream), "moe_w4a16_prepack")
     return packed
 

@@ -168,7 +168,8 @@ const char *moe_status_string(moe_status_t s) {
 moe_status_t moe_w4a16_prepack_size(int kind, int E, int N, int K, int group, size_t *bytes) {
     if (bytes) *bytes = 0;
     if (!bytes) return MOE_ERR_INVALID_ARG;
-    if ((kind != MOE_PACK_W13 && kind != MOE_PACK_W2) || group != kGroup || E < 1 || N <= 0 ||
+    if ((kind != MOE_PACK_W13 && kind != MOE_PACK_W2) ||
+        (group != 32 && group != 64 && group != 128) || E < 1 || N <= 0 ||
         K <= 0 || N % kTileRows || K % kChunkK || N > (1 << 20) || K > (1 << 20))
         return MOE_ERR_INVALID_ARG;
     *bytes = packed_bytes(E, N, K);
@@ -197,7 +198,8 @@ moe_status_t moe_w4a16_prepack(int kind, const uint8_t *q_canon, const uint16_t 
     h.E = E;
     h.N = N;
     h.K = K;
-    h.group = group;
+    h.group = kGroup;  // the packed blocks always hold one scale per 32 elements
+    h.source_group = group;
     h.status = MOE_OK;
     uint8_t *d = static_cast<uint8_t *>(dst);
     // a scale outside the exact range sets the header's status, which makes
@@ -206,7 +208,7 @@ moe_status_t moe_w4a16_prepack(int kind, const uint8_t *q_canon, const uint16_t 
     int32_t *wide = &reinterpret_cast<PackHeader *>(d)->wide_scales;
     if (cudaMemcpyAsync(d, &h, sizeof h, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         launch_prepack_codes(kind, q_canon, E, N, K, d, s) != cudaSuccess ||
-        launch_prepack_scales(kind, scales, E, N, K, d, flag, wide, s) != cudaSuccess ||
+        launch_prepack_scales(kind, scales, E, N, K, group, d, flag, wide, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;

@@ -51,7 +51,8 @@ struct PackHeader {
     int32_t E, N, K, group;
     int32_t status;   // MOE_OK once the prepack finished and validated
     int32_t wide_scales;  // nonzero: some |scale| > 65504/24 or infinite
-    int32_t pad[2];
+    int32_t source_group; // elements per scale of the source (32, 64, 128)
+    int32_t pad;
 };
 static_assert(sizeof(PackHeader) <= kHeaderBytes, "header too large");
 
@@ -146,7 +147,8 @@ constexpr int kFusedRouteMaxM = 64;
 // Both write into the blocks after the header of a prepacked buffer `dst`.
 cudaError_t launch_prepack_codes(int kind, const uint8_t *q, int E, int N, int K,
                                  uint8_t *dst, cudaStream_t s);
-cudaError_t launch_prepack_scales(int kind, const uint16_t *sc, int E, int N, int K,
+// `group`: elements of K per source scale (32, 64 or 128).
+cudaError_t launch_prepack_scales(int kind, const uint16_t *sc, int E, int N, int K, int group,
                                   uint8_t *dst, int32_t *bad_flag, int32_t *wide_flag,
                                   cudaStream_t s);
 

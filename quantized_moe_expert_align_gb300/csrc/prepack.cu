@@ -49,15 +49,17 @@ __global__ void prepack_codes_kernel(int kind, const uint32_t *__restrict__ q, i
     }
 }
 
-// One thread per output fp16 scale (the last 1 KiB of a block).  A scale
-// must be zero, NaN, infinite or of magnitude in [2^-14, 8188] so that
-// (q - 8) * scale is exact in fp16.  Scales above 65504/24 in magnitude or
-// infinite set *wide_flag: the one-instruction dequantisation needs -24 * s
-// in fp16.
+// One thread per output fp16 scale (the last 1 KiB of a block).  The block
+// holds one scale per 32 elements of K; a source with wider groups (64 or
+// 128 elements per scale) repeats each of its scales into the 32-element
+// slots it covers.  A scale must be zero, NaN, infinite or of magnitude in
+// [2^-14, 8188] so that (q - 8) * scale is exact in fp16.  Scales above
+// 65504/24 in magnitude or infinite set *wide_flag: the one-instruction
+// dequantisation needs -24 * s in fp16.
 __global__ void prepack_scales_kernel(int kind, const uint16_t *__restrict__ s, int E, int N,
-                                      int K, uint8_t *__restrict__ blocks, int32_t *bad_flag,
-                                      int32_t *wide_flag) {
-    const int tiles = N / kTileRows, chunks = K / kChunkK, groups = K / kGroup;
+                                      int K, int group, uint8_t *__restrict__ blocks,
+                                      int32_t *bad_flag, int32_t *wide_flag) {
+    const int tiles = N / kTileRows, chunks = K / kChunkK, groups = K / group;
     const int per_block = kTileRows * (kChunkK / kGroup);
     const int64_t total = (int64_t)E * tiles * chunks * per_block;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
@@ -69,7 +71,8 @@ __global__ void prepack_scales_kernel(int kind, const uint16_t *__restrict__ s, 
         const int tile = (int)((b / chunks) % tiles);
         const int64_t e = b / ((int64_t)chunks * tiles);
         const int n = canonical_row(kind, N, tile, r);
-        const float f = bf16_bits_to_float(__ldg(s + (e * N + n) * groups + chunk * 4 + g));
+        const int src = (chunk * kChunkK + g * kGroup) / group;
+        const float f = bf16_bits_to_float(__ldg(s + (e * N + n) * groups + src));
         const float a = fabsf(f);
         const bool ok = (f == 0.0f) || isnan(f) || isinf(f) ||
                         (a >= 6.103515625e-05f && a <= 8188.0f);
@@ -95,11 +98,12 @@ cudaError_t launch_prepack_codes(int kind, const uint8_t *q, int E, int N, int K
     return cudaGetLastError();
 }
 
-cudaError_t launch_prepack_scales(int kind, const uint16_t *sc, int E, int N, int K, uint8_t *dst,
-                                  int32_t *bad_flag, int32_t *wide_flag, cudaStream_t s) {
+cudaError_t launch_prepack_scales(int kind, const uint16_t *sc, int E, int N, int K, int group,
+                                  uint8_t *dst, int32_t *bad_flag, int32_t *wide_flag,
+                                  cudaStream_t s) {
     const int64_t n = (int64_t)E * (N / kTileRows) * (K / kChunkK) * (kScaleBlockBytes / 2);
-    prepack_scales_kernel<<<grid_for(n), 256, 0, s>>>(kind, sc, E, N, K, dst + kHeaderBytes,
-                                                      bad_flag, wide_flag);
+    prepack_scales_kernel<<<grid_for(n), 256, 0, s>>>(kind, sc, E, N, K, group,
+                                                      dst + kHeaderBytes, bad_flag, wide_flag);
     return cudaGetLastError();
 }
 

@@ -43,6 +43,7 @@ class Layer:
     H: int
     I: int
     k: int
+    group: int = GROUP   # elements of K per scale (32 on the pages; 64, 128 variants)
 
 
 @dataclass(frozen=True)
@@ -59,7 +60,12 @@ PLATEAU = Workload("plateau_e384_h7168_i2048_top8", Layer(384, 7168, 2048, 8), (
 PREFILL = Workload("prefill_zipf1.1_e384_h7168_i2048_top8", Layer(384, 7168, 2048, 8),
                    (4096, 16384), zipf_s=1.1)
 SECOND = Workload("second_e128_h4096_i1536_top8", Layer(128, 4096, 1536, 8), (1, 32, 256, 2048))
-WORKLOADS = {w.name: w for w in (TOY, DECODE, PLATEAU, PREFILL, SECOND)}
+# Variants beyond the pages' layer: 256 experts of the same width, and scale
+# groups of 128 elements on the second shape.
+E256 = Workload("e256_h7168_i2048_top8", Layer(256, 7168, 2048, 8), (1, 9, 90))
+GROUP128 = Workload("second_group128_e128_h4096_i1536_top8", Layer(128, 4096, 1536, 8, 128),
+                    (1, 32, 256))
+WORKLOADS = {w.name: w for w in (TOY, DECODE, PLATEAU, PREFILL, SECOND, E256, GROUP128)}
 
 
 def _rng(seed: int, tag: int, index: int = 0) -> np.random.Generator:
@@ -116,18 +122,18 @@ def packed_codes(N: int, K: int, seed: int, tag: int, e: int) -> np.ndarray:
     return bg.random_raw(nbytes // 8).view(np.uint8).reshape(N, K // 2)
 
 
-def scales(N: int, K: int, seed: int, tag: int, e: int) -> np.ndarray:
-    """[N][K/32] bf16 bit patterns, uniform on [0.002, 0.02]."""
+def scales(N: int, K: int, seed: int, tag: int, e: int, group: int = GROUP) -> np.ndarray:
+    """[N][K/group] bf16 bit patterns, uniform on [0.002, 0.02]."""
     g = _rng(seed, tag, e)
-    s = g.uniform(SCALE_LO, SCALE_HI, size=(N, K // GROUP)).astype(np.float32)
+    s = g.uniform(SCALE_LO, SCALE_HI, size=(N, K // group)).astype(np.float32)
     return f32_to_bf16_bits(s)
 
 
 def expert_weights(layer: Layer, e: int, seed: int = 0):
     """(w13[2I][H/2], s13[2I][H/32], w2[H][I/2], s2[H][I/32]) of expert e."""
-    H, I = layer.H, layer.I
-    return (packed_codes(2 * I, H, seed, TAG_W13, e), scales(2 * I, H, seed, TAG_S13, e),
-            packed_codes(H, I, seed, TAG_W2, e), scales(H, I, seed, TAG_S2, e))
+    H, I, g = layer.H, layer.I, layer.group
+    return (packed_codes(2 * I, H, seed, TAG_W13, e), scales(2 * I, H, seed, TAG_S13, e, g),
+            packed_codes(H, I, seed, TAG_W2, e), scales(H, I, seed, TAG_S2, e, g))
 
 
 def layer_weights(layer: Layer, seed: int = 0, experts: Optional[Sequence[int]] = None):
@@ -139,9 +145,9 @@ def layer_weights(layer: Layer, seed: int = 0, experts: Optional[Sequence[int]] 
 
     E, H, I = layer.E, layer.H, layer.I
     w13 = np.zeros((E, 2 * I, H // 2), np.uint8)
-    s13 = np.zeros((E, 2 * I, H // GROUP), np.uint16)
+    s13 = np.zeros((E, 2 * I, H // layer.group), np.uint16)
     w2 = np.zeros((E, H, I // 2), np.uint8)
-    s2 = np.zeros((E, H, I // GROUP), np.uint16)
+    s2 = np.zeros((E, H, I // layer.group), np.uint16)
 
     def fill(e):
         w13[e], s13[e], w2[e], s2[e] = expert_weights(layer, int(e), seed)

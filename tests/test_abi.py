@@ -50,7 +50,12 @@ def test_prepack_size(lib):
     assert st == moe.MOE_OK
     # header + int4 codes + one fp16 scale per 32 weights
     assert b == 256 + 384 * 4096 * 7168 // 2 + 384 * 4096 * (7168 // 32) * 2
-    for bad in [(3, 8, 256, 256, 32), (1, 8, 256, 256, 64), (1, 0, 256, 256, 32),
+    # wider scale groups are stored in the same layout: same size
+    for g in (64, 128):
+        st, b2 = moe.moe_w4a16_prepack_size(moe.MOE_PACK_W13, 384, 4096, 7168, g)
+        assert st == moe.MOE_OK and b2 == b
+    for bad in [(3, 8, 256, 256, 32), (1, 8, 256, 256, 16), (1, 8, 256, 256, 96),
+                (1, 8, 256, 256, 256), (1, 0, 256, 256, 32),
                 (1, 8, 200, 256, 32), (1, 8, 256, 96, 32)]:
         st, b = moe.moe_w4a16_prepack_size(*bad)
         assert st == moe.MOE_ERR_INVALID_ARG and b == 0
