@@ -324,7 +324,12 @@ def our_arm(args, wl):
     total_ms = max_over_ranks(sum(step_ms), "cuda")
     tokens_per_step = sum(wl.Ms)
     value = job_value(tokens_per_step, args.steps, world, total_ms)
-    gpu_launches = moe.moe_w4a16_get_diag()["kernels_launched"] * len(wl.Ms) * args.steps
+    launches_per_step = 0
+    for M in wl.Ms:   # kernels per call differ with M (small batches fuse two)
+        call(M)
+        launches_per_step += moe.moe_w4a16_get_diag()["kernels_launched"]
+    torch.cuda.synchronize()
+    gpu_launches = launches_per_step * args.steps
 
     # ---- per-kernel durations (events between the library's kernels) ----
     prof_steps = max(3, min(args.steps, 10))

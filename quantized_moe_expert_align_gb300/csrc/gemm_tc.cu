@@ -289,22 +289,37 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     // tiles g, g + G, g + 2G, ...: the CTAs then work on neighbouring tiles
     // at the same time, which share token rows (tiles of one token tile are
     // consecutive), so the token rows are read from L2, not DRAM.  With few
-    // tiles the chunks are cut into equal contiguous shares (stream-K).
+    // tiles, T = q G + rem: the chunks of tiles [0, rem) are cut into equal
+    // contiguous shares (stream-K), which each CTA does first, and then it
+    // takes q whole tiles rem + g, rem + g + G, ...  Every CTA thus ends on
+    // a whole tile, whose epilogue needs no fix-up: the ticketed reductions
+    // of split tiles happen while the other CTAs are still streaming.
     const int T = sm->bad ? 0 : sm->tile_prefix[a.E] * R;
     const bool rr = T >= 8 * G;
-    const int64_t W = (sm->bad || rr) ? 0 : (int64_t)T * KC;
+    const int q_whole = rr ? 0 : T / G;
+    const int rem = rr ? 0 : T - q_whole * G;
+    const int64_t W = (int64_t)rem * KC;  // stream-K units (tile * KC + chunk)
     const int64_t u_begin = range_begin(g, W, G), u_end = range_begin(g + 1, W, G);
-    const int my_chunks = rr ? (g < T ? (T - g + G - 1) / G : 0) * KC : (int)(u_end - u_begin);
-    const int tstep = rr ? G : 1;  // tile index step when a tile's K chunks are done
+    const int sk_chunks = (int)(u_end - u_begin);  // this CTA's stream-K chunks
+    const int my_chunks = rr ? (g < T ? (T - g + G - 1) / G : 0) * KC : sk_chunks + q_whole * KC;
     // tile and K chunk of this CTA's chunk number c
     auto locate_chunk = [&](int c, int &tile, int &kc) {
         if (rr) {
             tile = g + (c / KC) * G;
             kc = c % KC;
-        } else {
+        } else if (c < sk_chunks) {
             tile = (int)((u_begin + c) / KC);
             kc = (int)((u_begin + c) % KC);
+        } else {
+            tile = rem + g + ((c - sk_chunks) / KC) * G;
+            kc = (c - sk_chunks) % KC;
         }
+    };
+    // end (exclusive) of the run of chunks that starts at c and stays in one
+    // tile and one part of the schedule
+    auto segment_end = [&](int c, int kc) {
+        const int limit = (c < sk_chunks) ? sk_chunks : my_chunks;
+        return c + min(KC - kc, limit - c);
     };
 
     if (warp >= kProducerWarp && warp < kMmaWarp) {
@@ -338,37 +353,57 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             locate_chunk(c, tile, kc);
             locate();
         }
-        for (; c < my_chunks; c += NPROD) {
-            if (!warp_wait_bar(&sm->consumed[s], phase ^ 1, sm, a.ctrl, 1)) break;
-            if (elect_one()) {
-                // two copies per chunk: the weight block (codes and scales,
-                // contiguous) and the chunk's token rows
-                uint8_t *st = base + s * kStageBytes;
-                mbar_arrive_expect_tx(&sm->full[s], kStageBytes);
-                bulk_g2s_hint(st + kTokBoxes * kTokBox, a.w + kHeaderBytes + (blk0 + kc) * kBlockBytes,
-                              kBlockBytes, &sm->full[s], pol_w);
-                if (KIND == MOE_PACK_W13)
-                    tma_load_3d(st, &tok, 0, p0, 2 * kc, &sm->full[s]);
-                else if (kCat)  // [hi | lo] for K 0-63, then for K 64-127
-                    tma_load_4d(st, &tok, 0, p0, 0, 2 * kc, &sm->full[s]);
-                else            // [hi K0-63 | hi K64-127 | lo K0-63 | lo K64-127]
-                    tma_load_4d(st, &tok, 0, p0, 2 * kc, 0, &sm->full[s]);
+        // The loop is compiled once per schedule (a round-robin walk steps
+        // to the tile G further on without a lookup).
+        auto walk = [&](auto round_robin) {
+            constexpr bool kRR = decltype(round_robin)::value;
+            for (; c < my_chunks; c += NPROD) {
+                if (!warp_wait_bar(&sm->consumed[s], phase ^ 1, sm, a.ctrl, 1)) break;
+                if (elect_one()) {
+                    // two copies per chunk: the weight block (codes and
+                    // scales, contiguous) and the chunk's token rows
+                    uint8_t *st = base + s * kStageBytes;
+                    mbar_arrive_expect_tx(&sm->full[s], kStageBytes);
+                    bulk_g2s_hint(st + kTokBoxes * kTokBox,
+                                  a.w + kHeaderBytes + (blk0 + kc) * kBlockBytes, kBlockBytes,
+                                  &sm->full[s], pol_w);
+                    if (KIND == MOE_PACK_W13)
+                        tma_load_3d(st, &tok, 0, p0, 2 * kc, &sm->full[s]);
+                    else if (kCat)  // [hi | lo] for K 0-63, then for K 64-127
+                        tma_load_4d(st, &tok, 0, p0, 0, 2 * kc, &sm->full[s]);
+                    else            // [hi K0-63 | hi K64-127 | lo K0-63 | lo K64-127]
+                        tma_load_4d(st, &tok, 0, p0, 2 * kc, 0, &sm->full[s]);
+                }
+                __syncwarp();
+                s += NPROD;
+                if (s >= STAGES) {
+                    s -= STAGES;
+                    phase ^= 1;
+                }
+                // next chunk: K chunk + NPROD in the same tile unless that
+                // leaves the tile or (stream-K) the stream-K part
+                kc += NPROD;
+                if constexpr (kRR) {
+                    if (kc >= KC) {
+                        do {
+                            kc -= KC;
+                            tile += G;
+                        } while (kc >= KC);
+                        if (c + NPROD < my_chunks) locate();
+                    }
+                } else {
+                    const int cn = c + NPROD;
+                    if ((kc >= KC || (c < sk_chunks && cn >= sk_chunks)) && cn < my_chunks) {
+                        locate_chunk(cn, tile, kc);
+                        locate();
+                    }
+                }
             }
-            __syncwarp();
-            s += NPROD;
-            if (s >= STAGES) {
-                s -= STAGES;
-                phase ^= 1;
-            }
-            kc += NPROD;
-            if (kc >= KC) {
-                do {
-                    kc -= KC;
-                    tile += tstep;
-                } while (kc >= KC);
-                if (c + NPROD < my_chunks) locate();
-            }
-        }
+        };
+        if (rr)
+            walk(std::true_type{});
+        else
+            walk(std::false_type{});
         // Before the CTA exits, every copy issued must have landed; after an
         // abort elsewhere some were never consumed.  The last copy into each
         // stage is the only one that can be pending.  Chunks below c with
@@ -395,7 +430,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
         while (c < my_chunks && ok) {
             int tile, k0;
             locate_chunk(c, tile, k0);
-            const int k1 = min(KC, k0 + (my_chunks - c));
+            const int k1 = k0 + (segment_end(c, k0) - c);
             const Tile t = decode_tile<NT>(a, sm, tile);
             const int n_mma = kCat ? 2 * NT : max(16, (t.rows + 15) & ~15);
             const uint32_t idesc = idesc_f16_m128((uint32_t)n_mma);
@@ -538,7 +573,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
         for (int c_seg = 0; c_seg < my_chunks; ++seg) {
             int tile, k0;
             locate_chunk(c_seg, tile, k0);
-            const int k1 = min(KC, k0 + (my_chunks - c_seg));
+            const int k1 = k0 + (segment_end(c_seg, k0) - c_seg);
             const Tile t = decode_tile<NT>(a, sm, tile);
             const int acc = seg & 1;
             if (!warp_wait_bar(&sm->acc_full[acc], (seg >> 1) & 1, sm, a.ctrl, 6)) break;

@@ -45,8 +45,10 @@ def test_second_shape_small(e128_layer, M):
     _check(e128_layer, synth.SECOND, M)
 
 
-def test_deterministic(e128_layer):
-    x, ids, w = _inputs(synth.SECOND, 32)
+@pytest.mark.parametrize("M", [4, 32])
+def test_deterministic(e128_layer, M):
+    # M = 4: gather inside the alignment and combine inside the down GEMM
+    x, ids, w = _inputs(synth.SECOND, M)
     a, _ = e128_layer.forward(x, ids, w)
     b, _ = e128_layer.forward(x, ids, w)
     assert bool((a.view(-1) == b.view(-1)).all())
