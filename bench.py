@@ -53,15 +53,18 @@ TRAFFIC_CAPTURE = {
                          90: 5559540992 + 1870848},
     "profile": "profiles/dram_gemm_gate_up_decode_e384_m1_9_90.md",
 }
-KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "sm100.cuh", "moe_internal.h", "device_common.cuh"]
+KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "sm100.cuh", "moe_internal.h", "device_common.cuh",
+                  "schedule.cuh"]
 
 
 def kernel_sources_sha256():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_moe_expert_align_gb300", "csrc")
     for name in KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        path = os.path.join(csrc, name)
+        if os.path.exists(path):
+            with open(path, "rb") as f:
+                h.update(f.read())
     return h.hexdigest()
 
 
