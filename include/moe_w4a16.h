@@ -184,7 +184,10 @@ size_t moe_w4a16_workspace_size(int M, int k, int E, int H, int I);
  * The token-tile width (rows of expert-sorted tokens per tensor-core tile) is
  * chosen from M*k/E; for testing, the environment variable
  * MOE_W4A16_TOKEN_TILE = 16, 32, 64 or 128 fixes it (read once per process;
- * the workspace size follows it).
+ * the workspace size follows it).  For testing the failure path only,
+ * MOE_W4A16_TEST_NO_COPIES=1 (read once per process) makes the gate+up GEMM
+ * issue no copies: its bounded waits give up after about a second, the call
+ * reports MOE_ERR_DEVICE_TIMEOUT and its output is undefined.
  * Numerics: weights dequantised exactly to fp16, hidden converted to fp16
  * (values beyond fp16 range set MOE_ERR_DEVICE_FP16_RANGE), fp32
  * accumulation, the activation passed to the down GEMM as an fp16 hi+lo pair.

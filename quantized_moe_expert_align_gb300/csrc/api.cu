@@ -36,6 +36,17 @@ int pick_token_tile(int n, int E) {
     return nt;
 }
 
+// Failure-path test switch, read once per process:
+// MOE_W4A16_TEST_NO_COPIES=1 makes the gate+up GEMM issue no copies, so its
+// bounded waits run out and the call reports MOE_ERR_DEVICE_TIMEOUT.
+static int test_no_copies() {
+    static const int v = [] {
+        const char *e = std::getenv("MOE_W4A16_TEST_NO_COPIES");
+        return (e && std::atoi(e) == 1) ? 1 : 0;
+    }();
+    return v;
+}
+
 // The down GEMM's stage holds both halves (hi, lo) of its token rows, so a
 // 128-row tile leaves room for only two stages: it uses 64-row tiles there.
 int down_token_tile(int nt) {
@@ -377,7 +388,9 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     g1.act_hi = act_hi;
     g1.act_lo = act_lo;
     g1.ctrl = ctrl;
+    g1.test_no_copies = test_no_copies();
     TcArgs g2 = g1;
+    g2.test_no_copies = 0;
     g2.w = static_cast<const uint8_t *>(w2);
     g2.tickets = tickets + L.max_tok_tiles * r1;
     g2.tile_prefix = tile_prefix2;

@@ -400,10 +400,14 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                 }
             }
         };
-        if (rr)
+        if (a.test_no_copies) {
+            // failure-path test: no copy is issued (c stays below every
+            // chunk of this producer, so nothing is left in flight)
+        } else if (rr) {
             walk(std::true_type{});
-        else
+        } else {
             walk(std::false_type{});
+        }
         // Before the CTA exits, every copy issued must have landed; after an
         // abort elsewhere some were never consumed.  The last copy into each
         // stage is the only one that can be pending.  Chunks below c with

@@ -21,6 +21,10 @@ struct TcArgs {
     uint16_t *act_hi, *act_lo;   // gate+up output [n][I] fp16
     float *y;                    // down output [n][H] fp32
     Ctrl *ctrl;
+    // Failure-path test switch: nonzero makes the producers issue no copies,
+    // so the other roles' bounded waits run out (MOE_ERR_DEVICE_TIMEOUT) and
+    // the CTA winds down; zero in normal use.
+    int test_no_copies;
 };
 
 // Whether the down GEMM stacks the hi and lo rows of its activation into one

@@ -72,3 +72,48 @@ def test_m_zero_is_a_noop(toy_layer):
     moe.forward(x, ids, w, toy_layer.p13, toy_layer.p2,
                 L.E, L.I, out=out, workspace=ws)
     torch.cuda.synchronize()
+
+
+_STALL_CHILD = r"""
+import json, sys, time
+sys.path.insert(0, sys.argv[1])
+import numpy as np, torch
+import synth
+from tests import gpu_util as gu
+import quantized_moe_expert_align_gb300 as moe
+L = synth.TOY.layer
+dl = gu.DeviceLayer(L, 0)
+x = synth.hidden(4, L.H, 0)
+ids, w = synth.routing(4, L, 0)
+t0 = time.time()
+out, ws = dl.forward(x, ids, w)
+st, detail = moe.moe_w4a16_get_device_status(ws.buf)
+secs = time.time() - t0
+# the context is still usable afterwards
+y = (torch.arange(1024, device="cuda", dtype=torch.float32) * 2).sum().item()
+print(json.dumps({"status": st, "detail": detail, "secs": secs, "y": y}))
+"""
+
+
+def test_bounded_wait_runs_out(gpu):
+    """With the failure-path switch the gate+up GEMM issues no copies: its
+    waits give up after about a second, the status word says
+    MOE_ERR_DEVICE_TIMEOUT (detail: the role whose wait gave up), the kernel
+    winds down without hanging, and the CUDA context stays usable.  The
+    switch is read once per process, so in a child."""
+    import json
+    import os
+    import subprocess
+    import sys
+
+    import quantized_moe_expert_align_gb300 as moe
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, MOE_W4A16_TEST_NO_COPIES="1")
+    r = subprocess.run([sys.executable, "-c", _STALL_CHILD, root], env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    assert res["status"] == moe.MOE_ERR_DEVICE_TIMEOUT, res
+    assert 1 <= res["detail"] <= 6
+    assert res["y"] == float(sum(2 * i for i in range(1024)))
+    assert res["secs"] < 60
