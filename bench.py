@@ -47,10 +47,10 @@ KERNELS = ["align", "gather", "gemm_gate_up", "gemm_down", "combine"]
 # given (see the profile named there).  For any other source the figure no
 # longer describes the kernel and the bench reports traffic as null.
 TRAFFIC_CAPTURE = {
-    "sources_sha256": "0ecdcbdb5ab54b74c42764f9bfb6471f0672512bba907e2e81855c89fca40a78",
+    "sources_sha256": "12ea19f63b2df7038d32ac3e08134e0e10f7411bebcbcc72bad0f420eddd5d6a",
     "workload": "decode_e384_h7168_i2048_top8",
-    "bytes_per_launch": {1: 132319744 + 2771968, 9: 1091174144 + 545792,
-                         90: 5559696384 + 1926912},
+    "bytes_per_launch": {1: 132314112 + 2751232, 9: 1091143680 + 508416,
+                         90: 5559558144 + 1975040},
     "profile": "profiles/dram_gemm_gate_up_decode_e384_m1_9_90.md",
 }
 KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "sm100.cuh", "moe_internal.h", "device_common.cuh"]
@@ -410,6 +410,41 @@ def our_arm(args, wl):
                      "route_gbs": round(nbytes / (t_route / 1e3) / 1e9, 1),
                      "us_per_call_from_logits": round(1e3 * t_layer, 2)}
 
+    # ---- the same forward captured once in a CUDA graph and replayed (a
+    # decode loop without host launch overhead); L2 flushed before each
+    # replay, as in the timed steps ----
+    graph_us = {}
+    for M in wl.Ms:
+        x, ids, w, out = devb[M]
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            st = moe.moe_w4a16_forward(x, ids, w, p13, p2, out, M, L.k, L.E, L.H, L.I, ws.buf)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        if st != moe.MOE_OK:
+            raise moe.MoeError(st, "moe_w4a16_forward")
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            st = moe.moe_w4a16_forward(x, ids, w, p13, p2, out, M, L.k, L.E, L.H, L.I, ws.buf)
+        if st != moe.MOE_OK:
+            raise moe.MoeError(st, "moe_w4a16_forward (capture)")
+        graph.replay()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+        for r in range(reps):
+            flush.zero_()
+            ev[2 * r].record(stream)
+            graph.replay()
+            ev[2 * r + 1].record(stream)
+        torch.cuda.synchronize()
+        graph_us[M] = round(1e3 * float(np.mean([ev[2 * r].elapsed_time(ev[2 * r + 1])
+                                                   for r in range(reps)])), 2)
+        del graph
+    st, detail = moe.moe_w4a16_get_device_status(ws.buf)
+    if st != moe.MOE_OK:
+        raise moe.MoeError(st, f"graph replay device status (detail {detail})")
+
     # roofline: the gate+up GEMM streams the touched experts' w13 codes+scales
     b13, b2 = expert_bytes(L)
     sweep = []
@@ -432,6 +467,7 @@ def our_arm(args, wl):
             "frac_of_roofline_profiled": round(t_roof_ms / float(k_ms.sum()), 4),
             "pages_ms_rtx_pro_6000": PAGES_MS.get(M) if L.E == 384 else None,
             "router": router[M],
+            "us_per_call_graph": graph_us[M],
         })
     achieved = gemm1_bytes / (gemm1_ms / 1e3) / 1e9
     traffic = None

@@ -372,7 +372,7 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     al.r1 = r1;
     al.r2 = r2;
     al.off2 = L.max_tok_tiles * r1;
-    GatherArgs ga = {hidden, perm, offsets, n, k, H, E, xs, ctrl};
+    GatherArgs ga = {hidden, inv_perm, M, k, H, xs, ctrl};
     TcArgs g1 = {};
     g1.w = static_cast<const uint8_t *>(w13);
     g1.offsets = offsets;

@@ -1,6 +1,8 @@
 // elementwise.cu -- the two HBM-bound row kernels around the expert GEMMs:
-//   gather_hidden: xs[p] = fp16(hidden[perm[p] / k]), the hidden rows in
-//                  expert-sorted order as the gate+up GEMM's token operand;
+//   gather_hidden: xs[inv_perm[t*k + j]] = fp16(hidden[t]) for every slot j
+//                  of token t, the hidden rows in expert-sorted order as
+//                  the gate+up GEMM's token operand (each hidden row is
+//                  read once and written to its k sorted positions);
 //   combine:       out[t] = bf16(sum_{j ascending} topk_w[t][j] * y[inv_perm[t*k+j]]),
 //                  the fixed-order top-k combine back to token rows (the
 //                  "direct/scatter" row writes of "perf(exl3): accelerate
@@ -12,18 +14,17 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// One thread per 16-byte chunk (8 elements) of a sorted row.
+// One thread per 16-byte chunk (8 elements) of a token row: one read, one
+// conversion, k writes (slots whose id was invalid are skipped).
 __global__ void __launch_bounds__(kThreads) gather_hidden_kernel(GatherArgs a) {
     pdl_wait();
     pdl_trigger();
-    const int valid = __ldg(a.offsets + a.E);
     const int vecs = a.H / 8;
-    const int64_t total = (int64_t)valid * vecs;
+    const int64_t total = (int64_t)a.M * vecs;
     bool overflow = false;
     for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * kThreads) {
-        const int p = (int)(i / vecs), v = (int)(i % vecs);
-        const int t = __ldg(a.perm + p) / a.k;
+        const int t = (int)(i / vecs), v = (int)(i % vecs);
         const uint4 in = __ldg(reinterpret_cast<const uint4 *>(a.hidden + (size_t)t * a.H) + v);
         const uint32_t w[4] = {in.x, in.y, in.z, in.w};
         uint32_t o[4];
@@ -35,7 +36,11 @@ __global__ void __launch_bounds__(kThreads) gather_hidden_kernel(GatherArgs a) {
             const __half2 h = __floats2half2_rn(lo, hi);
             o[j] = *reinterpret_cast<const uint32_t *>(&h);
         }
-        reinterpret_cast<uint4 *>(a.xs + (size_t)p * a.H)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+        const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int j = 0; j < a.k; ++j) {
+            const int p = __ldg(a.inv_perm + (size_t)t * a.k + j);
+            if (p >= 0) reinterpret_cast<uint4 *>(a.xs + (size_t)p * a.H)[v] = ov;
+        }
     }
     if (overflow) set_status(a.ctrl, MOE_ERR_DEVICE_FP16_RANGE, 0);
 }
@@ -86,7 +91,7 @@ cudaError_t launch(Kernel k, const Args &args, int blocks, cudaStream_t s, bool 
 }  // namespace
 
 cudaError_t launch_gather_hidden(const GatherArgs &a, cudaStream_t s, bool pdl) {
-    int64_t blocks = ((int64_t)a.n * (a.H / 8) + kThreads - 1) / kThreads;
+    int64_t blocks = ((int64_t)a.M * (a.H / 8) + kThreads - 1) / kThreads;
     if (blocks > 152 * 16) blocks = 152 * 16;
     return launch(gather_hidden_kernel, a, (int)blocks, s, pdl);
 }

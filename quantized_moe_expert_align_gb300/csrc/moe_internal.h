@@ -153,11 +153,10 @@ cudaError_t launch_prepack_scales(int kind, const uint16_t *sc, int E, int N, in
                                   cudaStream_t s);
 
 struct GatherArgs {
-    const uint16_t *hidden;  // [M][H] bf16
-    const int32_t *perm;     // [n]
-    const int32_t *offsets;  // [E+1]; offsets[E] = valid rows
-    int n, k, H, E;
-    uint16_t *xs;            // [n][H] fp16
+    const uint16_t *hidden;    // [M][H] bf16
+    const int32_t *inv_perm;   // [M*k]: sorted row of each slot, -1 if invalid
+    int M, k, H;
+    uint16_t *xs;              // [n][H] fp16
     Ctrl *ctrl;
 };
 cudaError_t launch_gather_hidden(const GatherArgs &a, cudaStream_t s, bool pdl);
