@@ -54,10 +54,19 @@ int down_token_tile(int nt) {
     return (forced || nt <= 64) ? nt : 64;
 }
 
-AlignLayout align_layout(int, int, int) {
+AlignLayout align_layout(int M, int k, int E) {
     AlignLayout l;
     l.ctrl = 0;
-    l.total = sizeof(Ctrl);
+    l.seg_counts = l.seg_base = 0;
+    size_t off = sizeof(Ctrl);
+    if (align_large((int64_t)M * k)) {
+        const size_t seg = (size_t)E * kAlignSegs * 4;
+        l.seg_counts = off;
+        off = align_up(off + seg, 256);
+        l.seg_base = off;
+        off = align_up(off + seg, 256);
+    }
+    l.total = off;
     return l;
 }
 
@@ -76,6 +85,11 @@ FwdLayout fwd_layout(int M, int k, int E, int H, int I) {
         return at;
     };
     l.ctrl = take(sizeof(Ctrl));
+    l.seg_counts = l.seg_base = 0;
+    if (align_large((int64_t)n)) {
+        l.seg_counts = take((size_t)E * kAlignSegs * 4);
+        l.seg_base = take((size_t)E * kAlignSegs * 4);
+    }
     l.counts = take((size_t)E * 4);
     l.offsets = take((size_t)(E + 1) * 4);
     l.tile_prefix = take((size_t)(E + 1) * 4);
@@ -123,27 +137,40 @@ bool routing_sizes_ok(int M, int k, int E) {
     return M >= 0 && k >= 1 && k <= 64 && E >= 1 && E <= 1024 && (int64_t)M * k < INT_MAX;
 }
 
-// Routing ahead of the alignment kernel `a` (whose ids must be topk_ids):
-// small batches are routed by the alignment kernel itself, larger ones by
-// route_kernel first, after clearing the status word that the alignment
-// kernel then leaves alone.
-cudaError_t route_into(AlignArgs &a, const float *logits, int M, int k, int32_t *topk_ids,
-                       float *topk_w, cudaStream_t s) {
-    if (M <= kFusedRouteMaxM && route_vpl(a.E) <= kAlignRouteMaxVpl) {
-        a.logits = logits;
-        a.route_M = M;
-        a.route_k = k;
-        a.route_ids = topk_ids;
-        a.route_w = topk_w;
+// What precedes the alignment kernel(s) of `a` (whose ids must be topk_ids
+// when logits are given).  The single-CTA alignment kernel clears the status
+// word itself and routes small batches; otherwise the status word is cleared
+// by a memset first, then route_kernel routes (if logits are given), and the
+// alignment leaves the word alone.  Sets *route_kernel when it launched one.
+cudaError_t begin_call(AlignArgs &a, const float *logits, int M, int k, int32_t *topk_ids,
+                       float *topk_w, cudaStream_t s, bool *route_kernel = nullptr) {
+    const bool large = a.seg_counts != nullptr;
+    if (route_kernel) *route_kernel = false;
+    a.logits = nullptr;
+    if (!large && (!logits || (M <= kFusedRouteMaxM && route_vpl(a.E) <= kAlignRouteMaxVpl))) {
+        if (logits) {
+            a.logits = logits;
+            a.route_M = M;
+            a.route_k = k;
+            a.route_ids = topk_ids;
+            a.route_w = topk_w;
+        }
         a.reset_status = 1;
         return cudaSuccess;
     }
-    a.logits = nullptr;
     a.reset_status = 0;
-    cudaError_t err = cudaMemsetAsync(a.ctrl, 0, 2 * sizeof(int32_t), s);
-    if (err != cudaSuccess) return err;
+    cudaError_t err = cudaMemsetAsync(a.ctrl, 0, 4 * sizeof(int32_t), s);
+    if (err != cudaSuccess || !logits) return err;
+    if (route_kernel) *route_kernel = true;
     RouteArgs r = {logits, M, a.E, k, topk_ids, topk_w, a.ctrl};
     return launch_route(r, s);
+}
+
+// The large-batch workspace arrays of an alignment, when it takes that path.
+void set_segments(AlignArgs &a, uint8_t *ws, size_t seg_counts, size_t seg_base) {
+    const bool large = align_large(a.n);
+    a.seg_counts = large ? reinterpret_cast<int32_t *>(ws + seg_counts) : nullptr;
+    a.seg_base = large ? reinterpret_cast<int32_t *>(ws + seg_base) : nullptr;
 }
 
 bool layer_sizes_ok(int M, int k, int E, int H, int I) {
@@ -259,8 +286,13 @@ moe_status_t moe_align(const int32_t *ids, int M, int k, int E, int32_t *counts,
     a.perm = perm;
     a.inv_perm = inv_perm;
     a.tile_prefix = nullptr;
-    a.ctrl = reinterpret_cast<Ctrl *>(static_cast<uint8_t *>(workspace) + align_layout(M, k, E).ctrl);
-    if (launch_align(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    const AlignLayout L = align_layout(M, k, E);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.ctrl = reinterpret_cast<Ctrl *>(ws + L.ctrl);
+    set_segments(a, ws, L.seg_counts, L.seg_base);
+    if (begin_call(a, nullptr, M, k, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream)) !=
+            cudaSuccess ||
+        launch_align(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;
     }
@@ -282,8 +314,9 @@ moe_status_t moe_route_align(const float *logits, int M, int k, int E, int32_t *
     if (ws_bytes < align_layout(M, k, E).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
     moe_status_t st = check_device();
     if (st != MOE_OK) return st;
-    Ctrl *ctrl =
-        reinterpret_cast<Ctrl *>(static_cast<uint8_t *>(workspace) + align_layout(M, k, E).ctrl);
+    const AlignLayout L = align_layout(M, k, E);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(ws + L.ctrl);
     AlignArgs a = {};
     a.ids = topk_ids;
     a.n = M * k;
@@ -293,7 +326,8 @@ moe_status_t moe_route_align(const float *logits, int M, int k, int E, int32_t *
     a.perm = perm;
     a.inv_perm = inv_perm;
     a.ctrl = ctrl;
-    if (route_into(a, logits, M, k, topk_ids, topk_w, reinterpret_cast<cudaStream_t>(stream)) !=
+    set_segments(a, ws, L.seg_counts, L.seg_base);
+    if (begin_call(a, logits, M, k, topk_ids, topk_w, reinterpret_cast<cudaStream_t>(stream)) !=
             cudaSuccess ||
         launch_align(a, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
@@ -408,11 +442,10 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
 
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
     const bool pdl = (ev == nullptr);
-    const bool route_kernel =
-        logits && (M > kFusedRouteMaxM || route_vpl(E) > kAlignRouteMaxVpl);
-    if (logits &&
-        route_into(al, logits, M, k, const_cast<int32_t *>(ids), const_cast<float *>(topk_w), s) !=
-            cudaSuccess) {
+    bool route_kernel = false;
+    set_segments(al, ws, L.seg_counts, L.seg_base);
+    if (begin_call(al, logits, M, k, const_cast<int32_t *>(ids), const_cast<float *>(topk_w), s,
+                   &route_kernel) != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;
     }
@@ -432,7 +465,7 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     g_diag.token_tile = L.nt;
     g_diag.grid_gemm1 = grid;
     g_diag.grid_gemm2 = grid;
-    g_diag.kernels_launched = route_kernel ? 6 : 5;
+    g_diag.kernels_launched = 5 + (route_kernel ? 1 : 0) + (al.seg_counts ? 2 : 0);
     g_diag.workspace_bytes = (int64_t)L.total;
     g_diag.calls += 1;
     return MOE_OK;

@@ -75,7 +75,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Carving of the align workspace.
 struct AlignLayout {
-    size_t ctrl, total;
+    size_t ctrl, seg_counts, seg_base, total;  // seg_*: large batches only
 };
 AlignLayout align_layout(int M, int k, int E);
 
@@ -87,6 +87,7 @@ struct FwdLayout {
     int max_tok_tiles2; // bound on sum_e ceil(count_e / nt2)
     int grid;           // most CTAs the GEMM kernels may use (partials are sized for it)
     size_t ctrl, counts, offsets, tile_prefix, tile_prefix2, perm, inv_perm;
+    size_t seg_counts, seg_base;  // int32 [E][kAlignSegs] each, large batches only
     size_t tickets;     // int32 [max_tok_tiles * 4 * 2I/128 + max_tok_tiles2 * 4 * H/128]
     size_t partials;    // fp32 [grid][2][nt][128]
     size_t xs;          // [n][H] fp16 hidden rows in sorted order
@@ -128,8 +129,17 @@ struct AlignArgs {
     Ctrl *ctrl;
     int32_t *tickets; // if non-null: zero tiles*r1 entries at 0 and tiles2*r2 at off2
     int r1, r2, off2;
+    // Large batches (align_large): per-(expert, segment) counts and their
+    // exclusive prefixes, [E][kAlignSegs] int32 each; null for one CTA.  The
+    // caller clears the status word (and routes) before such a call.
+    int32_t *seg_counts, *seg_base;
 };
 cudaError_t launch_align(const AlignArgs &a, cudaStream_t s);
+// Batches of more than kAlignLargeSlots slots are aligned by kAlignSegs CTAs
+// (three kernels) instead of one.
+constexpr int kAlignSegs = 32;
+constexpr int kAlignLargeSlots = 1 << 14;
+inline bool align_large(int64_t n) { return n > kAlignLargeSlots; }
 
 // Router front-end: topk ids / weights from fp32 logits, one warp per token.
 struct RouteArgs {

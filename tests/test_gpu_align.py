@@ -66,3 +66,24 @@ def test_align_out_of_range_ids(gpu):
     st, detail, bad = _check(ids, 4)
     assert bad == 3
     assert st == moe.MOE_ERR_DEVICE_BAD_EXPERT_ID and detail in (4, -1, 1 << 30)
+
+
+def test_align_large_batches(gpu):
+    """More than 16384 slots take the multi-CTA path (per-segment counts,
+    one scan, per-segment placement): still the same stable counting sort,
+    out-of-range ids included."""
+    import quantized_moe_expert_align_gb300 as moe
+    rng = np.random.default_rng(11)
+    for ids, E in [(rng.integers(0, 384, size=(16385, 1)), 384),      # just above the switch
+                   (rng.integers(0, 1024, size=(3000, 8)), 1024),
+                   (np.zeros((5000, 4)), 1),
+                   (np.full((2100, 8), 17), 64),                      # one expert takes all
+                   (rng.integers(0, 7, size=(4099, 5)), 7)]:
+        st, _, bad = _check(np.asarray(ids, np.int32), E)
+        assert st == moe.MOE_OK and bad == 0
+    ids = rng.integers(0, 96, size=(2500, 8)).astype(np.int32)
+    ids[::97, 3] = -5
+    ids[5, 0] = 96
+    st, detail, bad = _check(ids, 96)
+    assert bad == 26 + 1
+    assert st == moe.MOE_ERR_DEVICE_BAD_EXPERT_ID and detail in (-5, 96)
