@@ -47,10 +47,10 @@ KERNELS = ["align", "gather", "gemm_gate_up", "gemm_down", "combine"]
 # given (see the profile named there).  For any other source the figure no
 # longer describes the kernel and the bench reports traffic as null.
 TRAFFIC_CAPTURE = {
-    "sources_sha256": "12ea19f63b2df7038d32ac3e08134e0e10f7411bebcbcc72bad0f420eddd5d6a",
+    "sources_sha256": "c91844521c74b246221111233aaea3f6c45172cdbd6d355d80b883ca16fcc096",
     "workload": "decode_e384_h7168_i2048_top8",
-    "bytes_per_launch": {1: 132314112 + 2751232, 9: 1091143680 + 508416,
-                         90: 5559558144 + 1975040},
+    "bytes_per_launch": {1: 132318976 + 2786048, 9: 1091142656 + 473344,
+                         90: 5559542784 + 1983232},
     "profile": "profiles/dram_gemm_gate_up_decode_e384_m1_9_90.md",
 }
 KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "sm100.cuh", "moe_internal.h", "device_common.cuh"]
