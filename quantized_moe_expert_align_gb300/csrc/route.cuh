@@ -61,8 +61,10 @@ __device__ __forceinline__ bool route_row(const float *row, int E, int k, int la
     }
     bad = __any_sync(0xffffffffu, bad);
 
-    // k rounds of a warp arg-max over (key, -index); the winner is cleared
-    // in its lane.  Slot j ends up in lane j % 32 (register a or b).
+    // k rounds of a warp arg-max over (key, -index): the largest key of the
+    // warp (one warp reduction), then the lowest index among the lanes that
+    // hold it (another); the winner is cleared in its lane.  Slot j ends up
+    // in lane j % 32 (register a or b).
     float la = 0.f, lb = 0.f;
     int ia = -1, ib = -1;
     for (int j = 0; j < k; ++j) {
@@ -74,15 +76,9 @@ __device__ __forceinline__ bool route_row(const float *row, int E, int k, int la
                 bk = key[i];
                 be = lane + 32 * i;
             }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const uint32_t ok = __shfl_xor_sync(0xffffffffu, bk, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (ok > bk || (ok == bk && oe < be)) {
-                bk = ok;
-                be = oe;
-            }
-        }
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        be = __reduce_min_sync(0xffffffffu, bk == mk ? be : 0x7FFFFFFF);
+        bk = mk;
         // (a select per register: an indexed store would put key[] in
         // local memory)
 #pragma unroll
