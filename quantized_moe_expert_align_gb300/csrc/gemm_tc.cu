@@ -53,7 +53,7 @@ constexpr int kEpiWarps = 4;
 __host__ __device__ constexpr int threads_for(int dq_groups, int producers, int mma_warps) {
     return 32 * (kEpiWarps + 4 * dq_groups + producers + mma_warps);
 }
-constexpr int kMaxABufs = 4;                  // TMEM A buffers (64 columns each)
+constexpr int kMaxABufs = 6;                  // TMEM A buffers (64 columns each)
 constexpr int kACols = kChunkK / 2;           // 64 fp16 pairs per row per chunk
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitCycles = 1ll << 31;  // bounded waits give up after ~1-2 s
@@ -233,7 +233,8 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     // into one B operand of 2*NT rows, so one MMA (whose cost does not grow
     // with N up to 128) covers both; the epilogue adds the two halves.
     constexpr bool kCat = (KIND == MOE_PACK_W2) && (NT <= 64);  // == stacked_hi_lo(NT)
-    constexpr int kAB = (STAGES >= 4) ? 4 : 2;               // TMEM A buffers in use
+    // TMEM A buffers in use (same rule as Config::kAB)
+    constexpr int kAB = (STAGES >= 4) ? (DQG > 4 ? DQG : 4) : 2;
     constexpr int kAccBase = kAB * kACols;
     constexpr int kAccCols = kCat ? 2 * NT : NT;              // columns per accumulator
     static_assert(kAccBase + 2 * MMAW * kAccCols <= 512, "tensor memory budget");
@@ -720,7 +721,13 @@ struct Config {
     // warpgroup always waits on the phase right after the one it consumed
     // and the parity test of the mbarrier cannot alias an older phase.
     static constexpr int kFit = (kBudget / kStage) < kMaxStages ? (kBudget / kStage) : kMaxStages;
-    static constexpr int kStages = kFit & ~1;
+    // Gate+up GEMM with small token tiles: 6 dequant warpgroups (1024
+    // threads, 64 registers each) over 12 stages.  The dequantisation is
+    // instruction-issue bound there, and 24 instead of 16 dequant warps issue
+    // more of the time (decode M = 90: 1026 -> 976 us); the down GEMM, whose
+    // epilogue needs more registers, spilled at 64 and stays at 4 groups.
+    static constexpr bool kWide = KIND == MOE_PACK_W13 && NT <= 32 && kFit >= 12;
+    static constexpr int kStages = kWide ? 12 : (kFit & ~1);
     // Warp roles.  Each mbarrier wait costs a shared-memory round trip of
     // over a hundred cycles even when the phase is complete, and every
     // instruction of the small control loops waits behind the dequantisation
@@ -732,8 +739,8 @@ struct Config {
     //  * two MMA issuers where N is small enough for the issue rate of
     //    tcgen05.mma, not the tensor pipe, to limit, and their
     //    accumulators fit next to the A buffers in tensor memory.
-    static constexpr int kDq = (kStages % 4 == 0) ? 4 : 2;
-    static constexpr int kAB = kStages >= 4 ? 4 : 2;
+    static constexpr int kDq = kWide ? 6 : ((kStages % 4 == 0) ? 4 : 2);
+    static constexpr int kAB = kStages >= 4 ? (kDq > 4 ? kDq : 4) : 2;
     static constexpr int kAccCols = (KIND == MOE_PACK_W2 && NT <= 64) ? 2 * NT : NT;
     static constexpr int kMma = (kAccCols <= 64 && kAB * kACols + 4 * kAccCols <= (int)kTmemCols)
                                     ? 2 : 1;
