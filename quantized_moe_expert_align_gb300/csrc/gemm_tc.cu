@@ -243,6 +243,12 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     static_assert(STAGES % kDqGroups == 0, "each stage must belong to one dequant group");
     static_assert(kAB % kDqGroups == 0, "each A buffer must belong to one dequant group");
     static_assert(STAGES % NPROD == 0, "each stage must belong to one producer");
+    // Each A buffer and each stage must also stay with one MMA issuer: an
+    // issuer that took turns on a buffer with the other could wait on its
+    // a_full barrier a whole phase ahead, where the parity test passes early
+    // (a down-GEMM build with 5 A buffers and 2 issuers ran into exactly
+    // that: its bounded waits gave up and reported MOE_ERR_DEVICE_TIMEOUT).
+    static_assert(kAB % MMAW == 0 && STAGES % MMAW == 0, "each A buffer must belong to one MMA warp");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
@@ -742,7 +748,9 @@ struct Config {
     static constexpr int kDq = kWide ? 6 : ((kStages % 4 == 0) ? 4 : 2);
     static constexpr int kAB = kStages >= 4 ? (kDq > 4 ? kDq : 4) : 2;
     static constexpr int kAccCols = (KIND == MOE_PACK_W2 && NT <= 64) ? 2 * NT : NT;
-    static constexpr int kMma = (kAccCols <= 64 && kAB * kACols + 4 * kAccCols <= (int)kTmemCols)
+    // (two issuers need the A buffers and stages to split evenly between them)
+    static constexpr int kMma = (kAccCols <= 64 && kAB * kACols + 4 * kAccCols <= (int)kTmemCols &&
+                                 kAB % 2 == 0 && kStages % 2 == 0)
                                     ? 2 : 1;
     static constexpr int kProd = 2;
     static constexpr int kThreads = threads_for(kDq, kProd, kMma);
