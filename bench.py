@@ -47,10 +47,10 @@ KERNELS = ["align", "gather", "gemm_gate_up", "gemm_down", "combine"]
 # given (see the profile named there).  For any other source the figure no
 # longer describes the kernel and the bench reports traffic as null.
 TRAFFIC_CAPTURE = {
-    "sources_sha256": "46bd6b64612459c1ca7132750a12317def856212077eb37384cffd5d0993db9f",
+    "sources_sha256": "3b5a2fda588113cfa9e1daaad0c60fe83deb15e178465a82af211c181ba380a5",
     "workload": "decode_e384_h7168_i2048_top8",
-    "bytes_per_launch": {1: 132317440 + 2809600, 9: 1091127552 + 464896,
-                         90: 5559694592 + 2083584},
+    "bytes_per_launch": {1: 132318720 + 2727424, 9: 1091280640 + 544000,
+                         90: 5559554816 + 1969408},
     "profile": "profiles/dram_gemm_gate_up_decode_e384_m1_9_90.md",
 }
 KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "sm100.cuh", "moe_internal.h", "device_common.cuh"]
