@@ -13,25 +13,30 @@
 // Design (weights as the MMA's M side, tokens as its N side):
 //  * One persistent CTA per SM.  The work is the list of tiles (expert,
 //    128-row weight tile, token tile of NT sorted rows) times 128-element K
-//    chunks; each CTA takes a contiguous, equal share of that list (stream-K),
-//    so the weight stream is spread evenly over all SMs even when only a few
-//    experts are active.  A tile cut between CTAs leaves fp32 partials in the
-//    workspace; the last CTA to finish it (an atomic ticket, no waiting)
-//    sums them in CTA order and runs the epilogue, so results do not depend
-//    on timing.
-//  * A TMA producer warp streams each chunk's 8 KiB code block and 1 KiB
-//    scale block (one bulk copy each) and the chunk's token rows (tensor
-//    copies, 128-byte swizzle) into a ring of shared-memory stages.
-//  * Two dequantisation warpgroups (alternating chunks) turn codes into
+//    chunks.  With many tiles each CTA takes whole tiles round-robin; with
+//    few, the chunks of the first tiles are cut into equal contiguous shares
+//    (stream-K), which each CTA does before its whole tiles, so the weight
+//    stream is spread evenly over all SMs even when only a few experts are
+//    active.  A tile cut between CTAs leaves fp32 partials in the workspace;
+//    the last CTA to finish it (an atomic ticket, no waiting) sums them in
+//    CTA order and runs the epilogue, so results do not depend on timing.
+//  * Two TMA producer warps (alternate chunks) stream each chunk's 9 KiB
+//    weight block (codes and scales, one bulk copy) and the chunk's token
+//    rows (one tensor copy, 128-byte swizzle) into a ring of shared-memory
+//    stages.
+//  * Dequantisation warpgroups (four, or six in the gate+up GEMM with small
+//    token tiles; each takes every fourth or sixth chunk) turn codes into
 //    exact fp16 weights, (q - 8) * scale, one weight row per thread, and
 //    write them straight into tensor memory with tcgen05.st.  That tensor
 //    memory is the A operand of tcgen05.mma, so dequantised weights never
 //    touch shared memory.
-//  * One thread issues tcgen05.mma (kind::f16, M = 128, N = token rows of the
-//    tile rounded up to 16, K = 16) accumulating in tensor memory; the down
-//    GEMM issues each step twice, for the hi and the lo halves of a.
-//  * An epilogue warpgroup drains the (double-buffered) accumulator while the
-//    next tile is being computed.
+//  * One or two MMA warps (alternate chunks, each with its own accumulator)
+//    issue tcgen05.mma (kind::f16, M = 128, N = token rows of the tile
+//    rounded up to 16, K = 16) from one elected thread, accumulating in
+//    tensor memory; the down GEMM multiplies the hi and the lo halves of a
+//    (stacked into one B operand for small token tiles).
+//  * An epilogue warpgroup drains the (double-buffered) accumulators while
+//    the next tile is being computed.
 // Every mbarrier wait is bounded; a wait that gives up records
 // MOE_ERR_DEVICE_TIMEOUT and the CTA winds down without hanging.
 #include <cstring>
@@ -740,7 +745,8 @@ struct Config {
     // warps' arithmetic, so the control roles are split over several warps
     // whose waits overlap:
     //  * four dequantisation warpgroups (each stage stays with one of them,
-    //    which needs a stage count divisible by four), else two;
+    //    which needs a stage count divisible by four), else two, or six over
+    //    12 stages in the gate+up GEMM with small token tiles (below);
     //  * two TMA producers (each owns every other stage);
     //  * two MMA issuers where N is small enough for the issue rate of
     //    tcgen05.mma, not the tensor pipe, to limit, and their
