@@ -47,10 +47,10 @@ KERNELS = ["align", "gather", "gemm_gate_up", "gemm_down", "combine"]
 # given (see the profile named there).  For any other source the figure no
 # longer describes the kernel and the bench reports traffic as null.
 TRAFFIC_CAPTURE = {
-    "sources_sha256": "3b5a2fda588113cfa9e1daaad0c60fe83deb15e178465a82af211c181ba380a5",
+    "sources_sha256": "4f5bb4b6a70ba879d67cf904ad58af1028fd17e16b4c6d43856d85c57fb16dee",
     "workload": "decode_e384_h7168_i2048_top8",
-    "bytes_per_launch": {1: 132318720 + 2727424, 9: 1091280640 + 544000,
-                         90: 5559554816 + 1969408},
+    "bytes_per_launch": {1: 132315904 + 2819072, 9: 1091143424 + 558592,
+                         90: 5559521792 + 1895680},
     "profile": "profiles/dram_gemm_gate_up_decode_e384_m1_9_90.md",
 }
 KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "sm100.cuh", "moe_internal.h", "device_common.cuh"]
