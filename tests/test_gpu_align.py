@@ -87,3 +87,24 @@ def test_align_large_batches(gpu):
     st, detail, bad = _check(ids, 96)
     assert bad == 26 + 1
     assert st == moe.MOE_ERR_DEVICE_BAD_EXPERT_ID and detail in (-5, 96)
+
+
+@pytest.mark.parametrize("M,k,E", [(37, 8, 384), (2500, 8, 96)])
+def test_align_without_inv_perm(gpu, M, k, E):
+    """inv_perm may be NULL (one CTA and the 32-CTA path): the rest is
+    unchanged."""
+    import torch
+    import quantized_moe_expert_align_gb300 as moe
+    rng = np.random.default_rng(M)
+    ids = rng.integers(0, E, size=(M, k)).astype(np.int32)
+    idd = torch.from_numpy(ids).cuda()
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(M * k, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(moe.moe_align_workspace_size(M, k, E), 256), dtype=torch.uint8,
+                     device="cuda")
+    assert moe.moe_align(idd, M, k, E, counts, offsets, perm, None, ws) == moe.MOE_OK
+    torch.cuda.synchronize()
+    rc, ro, rp, _, _ = oracle.align(ids, E)
+    assert np.array_equal(counts.cpu().numpy(), rc) and np.array_equal(offsets.cpu().numpy(), ro)
+    assert np.array_equal(perm.cpu().numpy(), rp)
