@@ -17,15 +17,23 @@ constexpr int kThreads = 256;
 // One thread per 16-byte chunk (8 elements) of a token row: one read, one
 // conversion, k writes (slots whose id was invalid are skipped).
 __global__ void __launch_bounds__(kThreads) gather_hidden_kernel(GatherArgs a) {
-    pdl_wait();
-    pdl_trigger();
     const int vecs = a.H / 8;
     const int64_t total = (int64_t)a.M * vecs;
+    const int64_t i0 = blockIdx.x * (int64_t)kThreads + threadIdx.x;
+    // The hidden rows are the call's input, complete before its first
+    // kernel started, so the first load goes out before waiting for the
+    // alignment (inv_perm is read only after the wait).
+    uint4 first = make_uint4(0, 0, 0, 0);
+    if (i0 < total)
+        first = __ldg(reinterpret_cast<const uint4 *>(a.hidden + (size_t)(i0 / vecs) * a.H) +
+                      i0 % vecs);
+    pdl_wait();
+    pdl_trigger();
     bool overflow = false;
-    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * kThreads) {
+    for (int64_t i = i0; i < total; i += (int64_t)gridDim.x * kThreads) {
         const int t = (int)(i / vecs), v = (int)(i % vecs);
-        const uint4 in = __ldg(reinterpret_cast<const uint4 *>(a.hidden + (size_t)t * a.H) + v);
+        const uint4 in = (i == i0) ? first
+                                   : __ldg(reinterpret_cast<const uint4 *>(a.hidden + (size_t)t * a.H) + v);
         const uint32_t w[4] = {in.x, in.y, in.z, in.w};
         uint32_t o[4];
 #pragma unroll
