@@ -55,12 +55,49 @@ __global__ void __launch_bounds__(kThreads) gather_hidden_kernel(GatherArgs a) {
 
 // One thread per 4 consecutive outputs of one token row.
 __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
-    pdl_wait();
-    pdl_trigger();
     const int quads = a.H / 4;
     const int64_t total = (int64_t)a.M * quads;
-    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * kThreads) {
+    const int64_t i0 = blockIdx.x * (int64_t)kThreads + threadIdx.x;
+    // Decode-sized batches (one output quad per thread, at most 8 slots):
+    // inv_perm (from the alignment, which had completed before the first
+    // GEMM could start) and topk_w (the call's input) are read before
+    // waiting for the down GEMM, so only the y loads wait.
+    constexpr int kPre = 8;
+    if (a.k <= kPre && total <= (int64_t)gridDim.x * kThreads && total <= 16384) {
+        int pos[kPre];
+        float w[kPre];
+        const int t = (int)(i0 / quads), q = (int)(i0 % quads);
+        if (i0 < total) {
+#pragma unroll
+            for (int j = 0; j < kPre; ++j) {
+                pos[j] = j < a.k ? __ldg(a.inv_perm + (size_t)t * a.k + j) : -1;
+                w[j] = j < a.k ? __ldg(a.topk_w + (size_t)t * a.k + j) : 0.f;
+            }
+        }
+        pdl_wait();
+        pdl_trigger();
+        if (i0 >= total) return;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < kPre; ++j) {
+            if (pos[j] < 0) continue;
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(a.y + (size_t)pos[j] * a.H) + q);
+            acc.x = fmaf(w[j], v.x, acc.x);
+            acc.y = fmaf(w[j], v.y, acc.y);
+            acc.z = fmaf(w[j], v.z, acc.z);
+            acc.w = fmaf(w[j], v.w, acc.w);
+        }
+        const __nv_bfloat162 b01 = __floats2bfloat162_rn(acc.x, acc.y);
+        const __nv_bfloat162 b23 = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 o;
+        o.x = *reinterpret_cast<const uint32_t *>(&b01);
+        o.y = *reinterpret_cast<const uint32_t *>(&b23);
+        reinterpret_cast<uint2 *>(a.out + (size_t)t * a.H)[q] = o;
+        return;
+    }
+    pdl_wait();
+    pdl_trigger();
+    for (int64_t i = i0; i < total; i += (int64_t)gridDim.x * kThreads) {
         const int t = (int)(i / quads), q = (int)(i % quads);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < a.k; ++j) {
