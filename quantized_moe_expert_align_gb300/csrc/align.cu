@@ -23,36 +23,6 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 
-// Exclusive scan of one int per thread over the whole block; returns the
-// thread's exclusive prefix and writes the block total to *total.
-__device__ int block_exclusive_scan(int v, int *warp_buf, int *total) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_buf[w] = x;
-    __syncthreads();
-    if (w == 0) {
-        int s = warp_buf[lane];
-        int incl = s;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        warp_buf[lane] = incl - s;
-        if (lane == 31) warp_buf[32] = incl;
-    }
-    __syncthreads();
-    int excl = warp_buf[w] + x - v;
-    *total = warp_buf[32];
-    __syncthreads();
-    return excl;
-}
-
 // Per-warp histogram of the flat slots [lo, hi) into row[E] (the warp's
 // row of the table); out-of-range ids are counted, not placed.
 __device__ __forceinline__ void warp_histogram(const AlignArgs &a, int32_t *row, int lo, int hi,
@@ -98,39 +68,91 @@ __device__ __forceinline__ void warp_place(const AlignArgs &a, int32_t *row, int
     }
 }
 
-// From each expert's count c (thread e < E): counts, offsets (the
-// warp-shuffle scan), both token-tile prefixes, and the zeroed split-K
-// tickets.  Returns the thread's offset; *total = offsets[E].
-__device__ int write_prefixes(const AlignArgs &a, int c, int *warp_buf, int *total) {
-    const int tid = threadIdx.x, E = a.E;
-    const int off = block_exclusive_scan(c, warp_buf, total);
-    if (tid < E) {
-        a.counts[tid] = c;
-        a.offsets[tid] = off;
-    }
-    if (tid == 0) a.offsets[E] = *total;
-    if (a.token_tile > 0) {
-        const int tiles = (tid < E) ? (c + a.token_tile - 1) / a.token_tile : 0;
-        int ttotal = 0;
-        const int toff = block_exclusive_scan(tiles, warp_buf, &ttotal);
-        if (tid < E) a.tile_prefix[tid] = toff;
-        if (tid == 0) a.tile_prefix[E] = ttotal;
-        const int tiles2 = (tid < E) ? (c + a.token_tile2 - 1) / a.token_tile2 : 0;
-        int ttotal2 = 0;
-        const int toff2 = block_exclusive_scan(tiles2, warp_buf, &ttotal2);
-        if (tid < E) a.tile_prefix2[tid] = toff2;
-        if (tid == 0) a.tile_prefix2[E] = ttotal2;
-        if (a.tickets) {
-            for (int i = tid; i < ttotal * a.r1; i += kThreads) a.tickets[i] = 0;
-            for (int i = tid; i < ttotal2 * a.r2; i += kThreads) a.tickets[a.off2 + i] = 0;
+// Exclusive scan of three ints per thread over the whole block at once (the
+// counts and the two token-tile counts): one warp-shuffle pass, then warps
+// 0..2 scan the 32 warp totals of x, y and z.  Returns the thread's
+// exclusive prefixes and writes the block totals to *total.  buf holds
+// 3 * 33 ints; the block has exactly 32 warps.
+__device__ int3 block_exclusive_scan3(int3 v, int *buf, int3 *total) {
+    static_assert(kWarps == 32, "warps 0..2 scan one warp total per lane");
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int3 x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int yx = __shfl_up_sync(0xffffffffu, x.x, o);
+        const int yy = __shfl_up_sync(0xffffffffu, x.y, o);
+        const int yz = __shfl_up_sync(0xffffffffu, x.z, o);
+        if (lane >= o) {
+            x.x += yx;
+            x.y += yy;
+            x.z += yz;
         }
     }
-    return off;
+    if (lane == 31) {
+        buf[w] = x.x;
+        buf[33 + w] = x.y;
+        buf[66 + w] = x.z;
+    }
+    __syncthreads();
+    if (w < 3) {  // warps 0, 1, 2 scan the warp totals of x, y, z
+        const int s = buf[33 * w + lane];
+        int incl = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        buf[33 * w + lane] = incl - s;
+        if (lane == 31) buf[33 * w + 32] = incl;
+    }
+    __syncthreads();
+    const int3 excl = make_int3(buf[w] + x.x - v.x, buf[33 + w] + x.y - v.y,
+                                buf[66 + w] + x.z - v.z);
+    *total = make_int3(buf[32], buf[65], buf[98]);
+    __syncthreads();
+    return excl;
+}
+
+// From each expert's count c (thread e < E): counts, offsets (the
+// warp-shuffle scan), both token-tile prefixes (scanned together with the
+// counts), and the zeroed split-K tickets.  Returns the thread's offset;
+// *total = offsets[E].
+__device__ int write_prefixes(const AlignArgs &a, int c, int *scan_buf, int *total) {
+    const int tid = threadIdx.x, E = a.E;
+    const bool tiled = a.token_tile > 0;
+    int3 v = make_int3(c, 0, 0);
+    if (tiled && tid < E) {
+        v.y = (c + a.token_tile - 1) / a.token_tile;
+        v.z = (c + a.token_tile2 - 1) / a.token_tile2;
+    }
+    int3 tot;
+    const int3 ex = block_exclusive_scan3(v, scan_buf, &tot);
+    *total = tot.x;
+    if (tid < E) {
+        a.counts[tid] = c;
+        a.offsets[tid] = ex.x;
+    }
+    if (tid == 0) a.offsets[E] = tot.x;
+    if (tiled) {
+        if (tid < E) {
+            a.tile_prefix[tid] = ex.y;
+            a.tile_prefix2[tid] = ex.z;
+        }
+        if (tid == 0) {
+            a.tile_prefix[E] = tot.y;
+            a.tile_prefix2[E] = tot.z;
+        }
+        if (a.tickets) {
+            for (int i = tid; i < tot.y * a.r1; i += kThreads) a.tickets[i] = 0;
+            for (int i = tid; i < tot.z * a.r2; i += kThreads) a.tickets[a.off2 + i] = 0;
+        }
+    }
+    return ex.x;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) align_kernel(AlignArgs a) {
     extern __shared__ int32_t table[];  // [kWarps][E]
-    __shared__ int warp_buf[33];
+    __shared__ int scan_buf[3 * 33];
     __shared__ int s_invalid;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int E = a.E, n = a.n;
@@ -180,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) align_kernel(AlignArgs a) {
         for (int ww = 0; ww < kWarps; ++ww) c += table[ww * E + tid];
     }
     int total = 0;
-    const int off = write_prefixes(a, c, warp_buf, &total);
+    const int off = write_prefixes(a, c, scan_buf, &total);
     if (tid < E) {
         // Phase B: starting position of (warp, expert) = offsets[e] + the
         // expert's slots in earlier segments.
@@ -242,7 +264,7 @@ __global__ void __launch_bounds__(kThreads) align_count_kernel(AlignArgs a, int3
 __global__ void __launch_bounds__(kThreads, 1) align_scan_kernel(AlignArgs a,
                                                                  const int32_t *seg_counts,
                                                                  int32_t *seg_base) {
-    __shared__ int warp_buf[33];
+    __shared__ int scan_buf[3 * 33];
     __shared__ int32_t s_count[1024];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, E = a.E;
     pdl_wait();
@@ -276,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) align_scan_kernel(AlignArgs a,
     __syncthreads();
     const int c = tid < E ? s_count[tid] : 0;
     int total = 0;
-    write_prefixes(a, c, warp_buf, &total);
+    write_prefixes(a, c, scan_buf, &total);
     for (int p = total + tid; p < a.n; p += kThreads) a.perm[p] = -1;
 }
 
