@@ -52,7 +52,9 @@ def test_align_edge_cases(gpu):
     for ids, E in [(np.array([[5]]), 8), (np.full((300, 8), 3), 384),
                    (rng.integers(0, 4, size=(77, 6)), 4), (np.zeros((50, 2)), 1),
                    (rng.integers(0, 1024, size=(999, 8)), 1024),
-                   (rng.integers(0, 384, size=(16384, 8)), 384)]:
+                   (rng.integers(0, 384, size=(16384, 8)), 384),
+                   (rng.integers(0, 384, size=(2048, 8)), 384),     # the one-CTA maximum
+                   (rng.integers(0, 5, size=(1111, 3)), 5)]:
         st, _, bad = _check(np.asarray(ids, np.int32), E)
         assert st == moe.MOE_OK and bad == 0
     # M = 0 writes zero counts/offsets
@@ -66,6 +68,14 @@ def test_align_out_of_range_ids(gpu):
     st, detail, bad = _check(ids, 4)
     assert bad == 3
     assert st == moe.MOE_ERR_DEVICE_BAD_EXPERT_ID and detail in (4, -1, 1 << 30)
+    # one CTA, segments of several 8-step batches with a ragged end
+    rng = np.random.default_rng(3)
+    ids = rng.integers(0, 200, size=(1500, 8)).astype(np.int32)
+    ids[::37, 2] = -3
+    ids[1499, 7] = 200
+    st, detail, bad = _check(ids, 200)
+    assert bad == len(range(0, 1500, 37)) + 1
+    assert st == moe.MOE_ERR_DEVICE_BAD_EXPERT_ID and detail in (-3, 200)
 
 
 def test_align_large_batches(gpu):
