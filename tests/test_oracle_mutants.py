@@ -38,6 +38,15 @@ MUTANTS = [
     ("router bad rows kept", "if (bad || mx == -INFINITY)", "if (mx == -INFINITY)"),
     ("router weight of the top slot everywhere", "(float)((exp((double)l[id[j]] - mx)",
      "(float)((exp((double)l[id[0]] - mx)"),
+    ("sigmoid instead of SiLU", "return v / (1.0 + exp(-v));", "return 1.0 / (1.0 + exp(-v));"),
+    ("scale row stride dropped", "s[n * (K / group) + kk / group]", "s[kk / group]"),
+    ("code row stride halved", "q[n * (K / 2) + kk / 2]", "q[n * (K / 4) + kk / 2]"),
+    ("down projection drops the last intermediate element",
+     "for (int64_t n = 0; n < I; ++n)\n                acc += a[n]",
+     "for (int64_t n = 0; n + 1 < I; ++n)\n                acc += a[n]"),
+    ("combine weight of slot 0 for every slot", "acc += (double)topk_w[t * k + j]",
+     "acc += (double)topk_w[t * k]"),
+    ("bf16 bits not shifted", "((uint32_t)bits) << 16", "((uint32_t)bits)"),
 ]
 
 
