@@ -44,10 +44,11 @@ KERNELS = ["align", "gather", "gemm_gate_up", "gemm_down", "combine"]
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum, one ncu pass,
 # caches flushed by ncu before each launch) of the gate+up GEMM launches of
 # the decode sweep, from one capture of the kernel sources whose SHA-256 is
-# given (see the profile named there).  For any other source the figure no
+# given (see the profile named there; the hash covers the sources' code with
+# comments and blank lines removed).  For any other source the figure no
 # longer describes the kernel and the bench reports traffic as null.
 TRAFFIC_CAPTURE = {
-    "sources_sha256": "4f5bb4b6a70ba879d67cf904ad58af1028fd17e16b4c6d43856d85c57fb16dee",
+    "sources_sha256": "901e484ff0c5ecfa6fed37872673523693baa9d8ed0bb1e84fc9822c2e079ec4",
     "workload": "decode_e384_h7168_i2048_top8",
     "bytes_per_launch": {1: 132315904 + 2819072, 9: 1091143424 + 558592,
                          90: 5559521792 + 1895680},
@@ -56,14 +57,42 @@ TRAFFIC_CAPTURE = {
 KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "sm100.cuh", "moe_internal.h", "device_common.cuh"]
 
 
+def code_only(text):
+    """C/C++ source without its comments: // and /* */ comments removed
+    (string and character literals kept as they are), each line stripped,
+    blank lines dropped.  Editing a comment leaves it unchanged; editing
+    code does not."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.strip() for line in "".join(out).split("\n"))
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_sources_sha256():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_moe_expert_align_gb300", "csrc")
     for name in KERNEL_SOURCES:
         path = os.path.join(csrc, name)
         if os.path.exists(path):
-            with open(path, "rb") as f:
-                h.update(f.read())
+            with open(path, encoding="utf-8") as f:
+                h.update(name.encode() + b"\0" + code_only(f.read()).encode() + b"\0")
     return h.hexdigest()
 
 

@@ -13,7 +13,7 @@ struct TcArgs {
     const uint8_t *w;            // prepacked weights (header included)
     const int32_t *offsets;      // [E+1] sorted-row offsets per expert
     const int32_t *tile_prefix;  // [E+1] token-tile prefix per expert (tile width nt)
-    int32_t *tickets;            // per (expert tile x weight tile); zeroed by align
+    int32_t *tickets;            // per (expert tile x weight tile); zeroed before the call's GEMMs
     float *partials;             // [grid][2][nt][128] fp32 split-tile partial sums
     int E, N, K, I;              // N, K of this matrix; I for the gate+up epilogue
     int kind;                    // MOE_PACK_W13 or MOE_PACK_W2
