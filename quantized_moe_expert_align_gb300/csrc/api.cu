@@ -4,6 +4,7 @@
 #include <cstdlib>
 #include <cstring>
 
+#include "elementwise.h"
 #include "gemm_tc.h"
 #include "moe_internal.h"
 #include "route.cuh"
@@ -402,11 +403,13 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     al.tile_prefix = tile_prefix;
     al.tile_prefix2 = tile_prefix2;
     al.ctrl = ctrl;
-    al.tickets = tickets;
+    al.tickets = nullptr;  // zeroed by the gather kernel (many CTAs), not the alignment
     al.r1 = r1;
     al.r2 = r2;
     al.off2 = L.max_tok_tiles * r1;
     GatherArgs ga = {hidden, inv_perm, M, k, H, xs, ctrl};
+    // every ticket of both GEMMs (the workspace's whole ticket region)
+    const TicketClear clear = {tickets, (int64_t)L.max_tok_tiles * r1 + (int64_t)L.max_tok_tiles2 * r2};
     TcArgs g1 = {};
     g1.w = static_cast<const uint8_t *>(w13);
     g1.offsets = offsets;
@@ -450,7 +453,7 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
         return MOE_ERR_CUDA;
     }
     if (mark(0) != cudaSuccess || launch_align(al, s) != cudaSuccess || mark(1) != cudaSuccess ||
-        launch_gather_hidden(ga, s, pdl) != cudaSuccess || mark(2) != cudaSuccess ||
+        launch_gather_hidden(ga, clear, s, pdl) != cudaSuccess || mark(2) != cudaSuccess ||
         launch_gemm_tc(g1, map_x, grid, s, pdl) != cudaSuccess || mark(3) != cudaSuccess ||
         launch_gemm_tc(g2, map_act, grid, s, pdl) != cudaSuccess || mark(4) != cudaSuccess ||
         launch_combine(cb, s, pdl) != cudaSuccess || mark(5) != cudaSuccess) {

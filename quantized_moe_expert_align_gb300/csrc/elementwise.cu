@@ -2,12 +2,14 @@
 //   gather_hidden: xs[inv_perm[t*k + j]] = fp16(hidden[t]) for every slot j
 //                  of token t, the hidden rows in expert-sorted order as
 //                  the gate+up GEMM's token operand (each hidden row is
-//                  read once and written to its k sorted positions);
+//                  read once and written to its k sorted positions); it
+//                  also zeroes the two GEMMs' split-K tickets;
 //   combine:       out[t] = bf16(sum_{j ascending} topk_w[t][j] * y[inv_perm[t*k+j]]),
 //                  the fixed-order top-k combine back to token rows (the
 //                  "direct/scatter" row writes of "perf(exl3): accelerate
 //                  fat-expert prefill - #77", "Engagement and fallback proof").
 #include "device_common.cuh"
+#include "elementwise.h"
 
 namespace moe {
 namespace {
@@ -16,10 +18,15 @@ constexpr int kThreads = 256;
 
 // One thread per 16-byte chunk (8 elements) of a token row: one read, one
 // conversion, k writes (slots whose id was invalid are skipped).
-__global__ void __launch_bounds__(kThreads) gather_hidden_kernel(GatherArgs a) {
+__global__ void __launch_bounds__(kThreads) gather_hidden_kernel(GatherArgs a, TicketClear z) {
     const int vecs = a.H / 8;
     const int64_t total = (int64_t)a.M * vecs;
     const int64_t i0 = blockIdx.x * (int64_t)kThreads + threadIdx.x;
+    // The tickets are used only by the two GEMMs, which read them after
+    // this kernel has completed, and nothing earlier in the call touches
+    // them: they are zeroed before the wait.
+    for (int64_t i = i0; i < z.n / 4; i += (int64_t)gridDim.x * kThreads)
+        reinterpret_cast<int4 *>(z.tickets)[i] = make_int4(0, 0, 0, 0);
     // The hidden rows are the call's input, complete before its first
     // kernel started, so the first load goes out before waiting for the
     // alignment (inv_perm is read only after the wait).
@@ -119,8 +126,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
     }
 }
 
-template <typename Kernel, typename Args>
-cudaError_t launch(Kernel k, const Args &args, int blocks, cudaStream_t s, bool pdl) {
+template <typename Kernel, typename... Args>
+cudaError_t launch(Kernel k, int blocks, cudaStream_t s, bool pdl, const Args &...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(blocks > 0 ? blocks : 1);
     cfg.blockDim = dim3(kThreads);
@@ -130,21 +137,26 @@ cudaError_t launch(Kernel k, const Args &args, int blocks, cudaStream_t s, bool 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k, args);
+    return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
 }  // namespace
 
-cudaError_t launch_gather_hidden(const GatherArgs &a, cudaStream_t s, bool pdl) {
+cudaError_t launch_gather_hidden(const GatherArgs &a, const TicketClear &clear, cudaStream_t s,
+                                 bool pdl) {
     int64_t blocks = ((int64_t)a.M * (a.H / 8) + kThreads - 1) / kThreads;
     if (blocks > 152 * 16) blocks = 152 * 16;
-    return launch(gather_hidden_kernel, a, (int)blocks, s, pdl);
+    return launch(gather_hidden_kernel, (int)blocks, s, pdl, a, clear);
+}
+
+cudaError_t launch_gather_hidden(const GatherArgs &a, cudaStream_t s, bool pdl) {
+    return launch_gather_hidden(a, TicketClear{nullptr, 0}, s, pdl);
 }
 
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s, bool pdl) {
     int64_t blocks = ((int64_t)a.M * (a.H / 4) + kThreads - 1) / kThreads;
     if (blocks > 152 * 16) blocks = 152 * 16;
-    return launch(combine_kernel, a, (int)blocks, s, pdl);
+    return launch(combine_kernel, (int)blocks, s, pdl, a);
 }
 
 }  // namespace moe
