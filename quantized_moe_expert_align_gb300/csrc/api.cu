@@ -403,10 +403,8 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     al.tile_prefix = tile_prefix;
     al.tile_prefix2 = tile_prefix2;
     al.ctrl = ctrl;
-    al.tickets = nullptr;  // zeroed by the gather kernel (many CTAs), not the alignment
-    al.r1 = r1;
-    al.r2 = r2;
-    al.off2 = L.max_tok_tiles * r1;
+    // al.tickets stays null: the gather kernel (many CTAs) zeroes the
+    // tickets, not the one-CTA alignment
     GatherArgs ga = {hidden, inv_perm, M, k, H, xs, ctrl};
     // every ticket of both GEMMs (the workspace's whole ticket region)
     const TicketClear clear = {tickets, (int64_t)L.max_tok_tiles * r1 + (int64_t)L.max_tok_tiles2 * r2};
@@ -429,7 +427,7 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     TcArgs g2 = g1;
     g2.test_no_copies = 0;
     g2.w = static_cast<const uint8_t *>(w2);
-    g2.tickets = tickets + L.max_tok_tiles * r1;
+    g2.tickets = tickets + (int64_t)L.max_tok_tiles * r1;
     g2.tile_prefix = tile_prefix2;
     g2.nt = L.nt2;
     g2.N = H;
