@@ -253,7 +253,12 @@ moe_status_t moe_w4a16_forward_profiled(const uint16_t *hidden, const int32_t *t
  *    H=7168, I=2048, top-8 that admits M up to about 24 tokens).
  *  - The first call on a device looks up the array's device address (once
  *    per device, with that device current); make that first call before
- *    any stream capture.
+ *    any stream capture.  The address is kept for the life of the process:
+ *    after cudaDeviceReset the library's device code is loaded again and
+ *    the array may move, so do not call this entry point on a device that
+ *    was reset after its first call.
+ *  - Devices with an ordinal of 64 or more are not supported: the call
+ *    returns MOE_ERR_UNSUPPORTED_DEVICE.
  *  - Every call on a device shares the one array and it keeps the last
  *    call's contents; the call itself resets what must start at zero (the
  *    status word and the split-K tickets).  Calls that overlap on the GPU
@@ -295,7 +300,12 @@ typedef struct {
 moe_status_t moe_w4a16_workspace_views(int M, int k, int E, int H, int I,
                                        moe_ws_views_t *views);
 
-/* Diagnostics of the most recent forward call issued from this process. */
+/*
+ * Diagnostics of the most recent forward call issued from the calling host
+ * thread (each thread keeps its own record, so calls from other threads or
+ * for other devices do not change it); `calls` counts that thread's forward
+ * calls.
+ */
 typedef struct {
     int32_t version;          /* 1 */
     int32_t M, k, E, H, I;

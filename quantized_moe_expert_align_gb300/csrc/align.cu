@@ -114,9 +114,8 @@ __device__ int3 block_exclusive_scan3(int3 v, int *buf, int3 *total) {
 }
 
 // From each expert's count c (thread e < E): counts, offsets (the
-// warp-shuffle scan), both token-tile prefixes (scanned together with the
-// counts), and the zeroed split-K tickets.  Returns the thread's offset;
-// *total = offsets[E].
+// warp-shuffle scan) and both token-tile prefixes (scanned together with the
+// counts).  Returns the thread's offset; *total = offsets[E].
 __device__ int write_prefixes(const AlignArgs &a, int c, int *scan_buf, int *total) {
     const int tid = threadIdx.x, E = a.E;
     const bool tiled = a.token_tile > 0;
@@ -141,10 +140,6 @@ __device__ int write_prefixes(const AlignArgs &a, int c, int *scan_buf, int *tot
         if (tid == 0) {
             a.tile_prefix[E] = tot.y;
             a.tile_prefix2[E] = tot.z;
-        }
-        if (a.tickets) {
-            for (int i = tid; i < tot.y * a.r1; i += kThreads) a.tickets[i] = 0;
-            for (int i = tid; i < tot.z * a.r2; i += kThreads) a.tickets[a.off2 + i] = 0;
         }
     }
     return ex.x;

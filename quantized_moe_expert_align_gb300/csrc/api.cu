@@ -111,7 +111,9 @@ FwdLayout fwd_layout(int M, int k, int E, int H, int I) {
 
 namespace {
 
-moe_diag_t g_diag = {1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+// Per host thread: calls from several threads (or for several devices from
+// several threads) never write the same record.
+thread_local moe_diag_t g_diag = {1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -403,8 +405,8 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     al.tile_prefix = tile_prefix;
     al.tile_prefix2 = tile_prefix2;
     al.ctrl = ctrl;
-    // al.tickets stays null: the gather kernel (many CTAs) zeroes the
-    // tickets, not the one-CTA alignment
+    // The gather kernel (hundreds of CTAs) zeroes both GEMMs' split-K
+    // tickets, not the one-CTA alignment.
     GatherArgs ga = {hidden, inv_perm, M, k, H, xs, ctrl};
     // every ticket of both GEMMs (the workspace's whole ticket region)
     const TicketClear clear = {tickets, (int64_t)L.max_tok_tiles * r1 + (int64_t)L.max_tok_tiles2 * r2};

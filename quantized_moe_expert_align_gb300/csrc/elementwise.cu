@@ -22,9 +22,13 @@ __global__ void __launch_bounds__(kThreads) gather_hidden_kernel(GatherArgs a, T
     const int vecs = a.H / 8;
     const int64_t total = (int64_t)a.M * vecs;
     const int64_t i0 = blockIdx.x * (int64_t)kThreads + threadIdx.x;
-    // The tickets are used only by the two GEMMs, which read them after
-    // this kernel has completed, and nothing earlier in the call touches
-    // them: they are zeroed before the wait.
+    // The tickets are used only by the two GEMMs' epilogue warps, and
+    // nothing earlier in the call touches them, so they are zeroed before
+    // the wait.  An epilogue warp's first ticket update follows its CTA's
+    // first accumulator, which follows the producers' griddepcontrol.wait
+    // (through the stage and accumulator mbarriers), and that wait returns
+    // only once this kernel has completed.  A change that lets the GEMMs
+    // touch a ticket before that chain would race with these stores.
     for (int64_t i = i0; i < z.n / 4; i += (int64_t)gridDim.x * kThreads)
         reinterpret_cast<int4 *>(z.tickets)[i] = make_int4(0, 0, 0, 0);
     // The hidden rows are the call's input, complete before its first
@@ -147,10 +151,6 @@ cudaError_t launch_gather_hidden(const GatherArgs &a, const TicketClear &clear, 
     int64_t blocks = ((int64_t)a.M * (a.H / 8) + kThreads - 1) / kThreads;
     if (blocks > 152 * 16) blocks = 152 * 16;
     return launch(gather_hidden_kernel, (int)blocks, s, pdl, a, clear);
-}
-
-cudaError_t launch_gather_hidden(const GatherArgs &a, cudaStream_t s, bool pdl) {
-    return launch_gather_hidden(a, TicketClear{nullptr, 0}, s, pdl);
 }
 
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s, bool pdl) {

@@ -676,6 +676,10 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             if (!whole) {
                 // Fixed-order reduction by whichever CTA finishes the tile
                 // last; each warp handles its own 32 rows with its own ticket.
+                // The previous kernel of the call (the hidden-row gather)
+                // zeroes the tickets: this atomic must stay ordered after the
+                // producers' griddepcontrol.wait, which it is through the
+                // full -> MMA -> acc_full chain that led here.
                 const int64_t tu0 = (int64_t)tile * KC, tu1 = tu0 + KC - 1;
                 const int ncontrib = contributors(tu0, tu1, W, G);
                 __threadfence();

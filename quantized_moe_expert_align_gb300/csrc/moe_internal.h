@@ -127,8 +127,6 @@ struct AlignArgs {
     int token_tile2;  //     and tile_prefix2 for this one
     int32_t *counts, *offsets, *perm, *inv_perm, *tile_prefix, *tile_prefix2;
     Ctrl *ctrl;
-    int32_t *tickets; // if non-null: zero tiles*r1 entries at 0 and tiles2*r2 at off2
-    int r1, r2, off2;
     // Large batches (align_large): per-(expert, segment) counts and their
     // exclusive prefixes, [E][kAlignSegs] int32 each; null for one CTA.  The
     // caller clears the status word (and routes) before such a call.
@@ -169,8 +167,6 @@ struct GatherArgs {
     uint16_t *xs;              // [n][H] fp16
     Ctrl *ctrl;
 };
-cudaError_t launch_gather_hidden(const GatherArgs &a, cudaStream_t s, bool pdl);
-
 
 struct CombineArgs {
     const float *y;           // [n][H]
