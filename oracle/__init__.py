@@ -126,8 +126,10 @@ class Oracle:
         from the scale shapes [E][N][K/group].
 
         Returns ``out`` [M][H] float64, or with ``want_intermediates`` a dict
-        with ``out``, ``act`` ([M*k][I], sorted order), ``y`` ([M*k][H],
-        sorted order) and the alignment.
+        with ``out``, ``act`` ([n_valid][I], sorted order), ``y``
+        ([n_valid][H], sorted order) and the alignment, n_valid being the
+        number of slots whose id lies in [0, E) (the rows the alignment
+        places; slots with other ids are left out of every stage).
         """
         hidden = np.ascontiguousarray(hidden, dtype=np.uint16)
         ids = np.ascontiguousarray(ids, dtype=np.int32)
@@ -141,9 +143,11 @@ class Oracle:
         assert w13.dtype == np.uint8 and w2.dtype == np.uint8
         assert s13.dtype == np.uint16 and s2.dtype == np.uint16
         n = M * k
+        # only the placed slots get sorted rows: size y and act by them
+        n_valid = int(np.count_nonzero((ids >= 0) & (ids < E)))
         out = np.zeros((M, H), np.float64)
-        y = np.zeros((max(n, 1), H), np.float64)
-        act = np.zeros((max(n, 1), I), np.float64) if want_intermediates else None
+        y = np.zeros((max(n_valid, 1), H), np.float64)
+        act = np.zeros((max(n_valid, 1), I), np.float64) if want_intermediates else None
         nt = self.num_threads()
         scratch = np.zeros(nt * I, np.float64)
         counts = np.zeros(E, np.int32)
@@ -158,7 +162,7 @@ class Oracle:
             raise RuntimeError("oracle_forward: scratch too small")
         if not want_intermediates:
             return out
-        return {"out": out, "act": act[:n], "y": y[:n], "counts": counts,
+        return {"out": out, "act": act[:n_valid], "y": y[:n_valid], "counts": counts,
                 "offsets": offsets, "perm": perm[:n], "inv_perm": inv_perm[:n],
                 "n_invalid": int(bad)}
 

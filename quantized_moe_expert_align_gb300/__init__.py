@@ -193,31 +193,6 @@ def moe_w4a16_workspace_views(M, k, E, H, I):
     return {name: getattr(v, name) for name, _ in moe_ws_views_t._fields_}
 
 
-def intermediates(workspace, M, k, E, H, I):
-    """Copies of the sorted intermediates a finished forward left in its
-    workspace: dict of numpy arrays (counts, offsets, perm, inv_perm,
-    act = hi + lo as float64 [valid][I], y [valid][H])."""
-    import numpy as np
-    import torch
-    ws = workspace.buf if isinstance(workspace, Workspace) else workspace
-    v = moe_w4a16_workspace_views(M, k, E, H, I)
-    n = M * k
-
-    def view(off, count, dtype):
-        nbytes = count * torch.empty((), dtype=dtype).element_size()
-        return ws[off:off + nbytes].view(dtype).cpu().numpy()
-
-    torch.cuda.synchronize()
-    offsets = view(v["offsets"], E + 1, torch.int32)
-    valid = int(offsets[E])
-    hi = view(v["act_hi"], n * I, torch.float16).reshape(n, I)[:valid].astype(np.float64)
-    lo = view(v["act_lo"], n * I, torch.float16).reshape(n, I)[:valid].astype(np.float64)
-    return {"counts": view(v["counts"], E, torch.int32), "offsets": offsets,
-            "perm": view(v["perm"], n, torch.int32), "inv_perm": view(v["inv_perm"], n, torch.int32),
-            "act": hi + lo, "act_hi": hi,
-            "y": view(v["y"], n * H, torch.float32).reshape(n, H)[:valid].astype(np.float64)}
-
-
 def moe_w4a16_get_diag():
     d = moe_diag_t()
     st = load().moe_w4a16_get_diag(ctypes.byref(d))

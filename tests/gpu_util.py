@@ -96,3 +96,130 @@ def sample_rows(M: int, count: int, seed: int = 1) -> np.ndarray:
     rng = np.random.default_rng(seed)
     mid = rng.choice(np.arange(1, M - 1), size=count - 2, replace=False)
     return np.sort(np.concatenate([[0, M - 1], mid]))
+
+
+# ---------------------------------------------------------------------------
+# Stage-level checks: the sorted intermediates a finished forward leaves in its
+# workspace (act = silu(gate)*up as an fp16 hi + lo pair, y the down
+# projection, both per expert-sorted row) against the oracle's, slot by slot.
+# ---------------------------------------------------------------------------
+STAGE_ATOL = 1e-3   # |gpu - oracle| <= STAGE_ATOL + STAGE_RTOL * |oracle| for act and y
+STAGE_RTOL = 1e-3
+
+
+def workspace_rows(ws_buf, M, k, E, H, I, rows):
+    """Copies from a finished forward's workspace: the alignment arrays
+    (counts, offsets, perm, inv_perm, whole) and the sorted rows ``rows`` of
+    act_hi, act_lo and y, as float64 numpy arrays (rows picked on the device,
+    so a large batch's intermediates are never copied whole)."""
+    import quantized_moe_expert_align_gb300 as moe
+    torch = torch_mod()
+    v = moe.moe_w4a16_workspace_views(M, k, E, H, I)
+    n = M * k
+    torch.cuda.synchronize()
+
+    def whole(off, count, dtype):
+        nbytes = count * torch.empty((), dtype=dtype).element_size()
+        return ws_buf[off:off + nbytes].view(dtype)
+
+    idx = torch.from_numpy(np.ascontiguousarray(rows, dtype=np.int64)).to(ws_buf.device)
+
+    def pick(off, cols, dtype):
+        t = whole(off, n * cols, dtype).view(n, cols)
+        return t.index_select(0, idx).cpu().numpy().astype(np.float64)
+
+    return {"counts": whole(v["counts"], E, torch.int32).cpu().numpy(),
+            "offsets": whole(v["offsets"], E + 1, torch.int32).cpu().numpy(),
+            "perm": whole(v["perm"], n, torch.int32).cpu().numpy(),
+            "inv_perm": whole(v["inv_perm"], n, torch.int32).cpu().numpy(),
+            "act_hi": pick(v["act_hi"], I, torch.float16),
+            "act_lo": pick(v["act_lo"], I, torch.float16),
+            "y": pick(v["y"], H, torch.float32)}
+
+
+def oracle_on_slots(dl, x, ids, w, slots):
+    """The oracle's forward restricted to the flat slots ``slots`` (t*k + j):
+    it runs on the tokens that own them, with every other slot's id set to
+    -1 (such a slot is left out of the alignment and of every stage), so it
+    computes act and y of exactly those slots.  Returns (slots sorted,
+    oracle dict, the oracle's sorted row of each slot)."""
+    import oracle
+    L = dl.layer
+    k = L.k
+    slots = np.unique(np.asarray(slots, np.int64))
+    toks, tpos = np.unique(slots // k, return_inverse=True)
+    keep = np.zeros((len(toks), k), bool)
+    keep[tpos, slots % k] = True
+    ids_m = np.where(keep, ids[toks], -1).astype(np.int32)
+    ref = oracle.forward(x[toks], ids_m, w[toks], dl.w13, dl.s13, dl.w2, dl.s2,
+                         L.E, L.H, L.I, want_intermediates=True)
+    ref_pos = ref["inv_perm"].reshape(len(toks), k)[tpos, slots % k]
+    assert np.all(ref_pos >= 0)
+    return slots, ref, ref_pos, toks
+
+
+def check_stages(dl, x, ids, w, ws_buf, slots, what=""):
+    """Alignment bit-exact against the oracle's (whole batch), then act and y
+    of every slot in ``slots`` element by element.  Returns the oracle dict
+    of the restricted run (its ``out`` holds the tokens that own the slots,
+    complete only for tokens whose every slot is in ``slots``)."""
+    import oracle
+    L = dl.layer
+    M, k = ids.shape
+    rc, ro, rp, rip, _ = oracle.align(ids, L.E)
+    slots, ref, ref_pos, toks = oracle_on_slots(dl, x, ids, w, slots)
+    gpu_pos = rip[slots]
+    g = workspace_rows(ws_buf, M, k, L.E, L.H, L.I, gpu_pos)
+    assert np.array_equal(g["counts"], rc), f"{what}: counts"
+    assert np.array_equal(g["offsets"], ro), f"{what}: offsets"
+    n = int(ro[L.E])
+    assert np.array_equal(g["perm"][:n], rp[:n]), f"{what}: perm"
+    assert np.array_equal(g["inv_perm"], rip), f"{what}: inv_perm"
+    for name, got, exp in [("act", g["act_hi"] + g["act_lo"], ref["act"][ref_pos]),
+                           ("y", g["y"], ref["y"][ref_pos])]:
+        assert np.all(np.isfinite(got)), f"{what}: non-finite {name}"
+        d = np.abs(got - exp)
+        tol = STAGE_ATOL + STAGE_RTOL * np.abs(exp)
+        bad = d > tol
+        if np.any(bad):
+            r, c = np.argwhere(bad)[0]
+            raise AssertionError(
+                f"{what}: {name}: {int(bad.sum())} elements out of tolerance in "
+                f"{int(bad.any(axis=1).sum())} of {len(slots)} slots; first at slot "
+                f"{int(slots[r])} (sorted row {int(gpu_pos[r])}), column {int(c)}: "
+                f"{got[r, c]!r} vs {exp[r, c]!r}; max d/tol {float(np.max(d / tol)):.3f}")
+    return ref, toks
+
+
+def tile_sample(ids, E, nt, nt2, heavy_full=1, heavy_edges=4):
+    """Slots chosen from the token-tile structure of both GEMMs: the first and
+    last sorted row of every token tile (tiles of ``nt`` rows for the gate+up
+    GEMM and ``nt2`` for the down GEMM, per expert segment), every row of the
+    ``heavy_full`` heaviest experts, and every row of the first and last
+    token tile of the ``heavy_edges`` heaviest experts (the last being the
+    partial one).  Returns flat slot indices."""
+    import oracle
+    counts, offsets, perm, _, _ = oracle.align(ids, E)
+    rows = set()
+    for e in np.nonzero(counts)[0]:
+        c, o = int(counts[e]), int(offsets[e])
+        for width in (nt, nt2):
+            for s in range(0, c, width):
+                rows.add(o + s)
+                rows.add(o + min(s + width, c) - 1)
+    order = np.argsort(-counts, kind="stable")
+    for e in order[:heavy_full]:
+        rows.update(range(int(offsets[e]), int(offsets[e + 1])))
+    for e in order[:heavy_edges]:
+        c, o = int(counts[e]), int(offsets[e])
+        last = (c - 1) // nt * nt
+        rows.update(range(o, o + min(nt, c)))
+        rows.update(range(o + last, o + c))
+    return perm[np.array(sorted(rows), np.int64)]
+
+
+def down_tile(nt):
+    """Token rows per tile of the down GEMM for a gate+up tile of ``nt`` rows
+    (the library caps it at 64: its stages hold both halves of the
+    activation)."""
+    return nt if nt <= 64 else 64

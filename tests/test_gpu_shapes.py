@@ -19,7 +19,8 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _run(L, M, seed=0, sample=None):
+def _run(L, M, seed=0):
+    """The whole batch: every token's output and every slot's act and y."""
     import quantized_moe_expert_align_gb300 as moe
     dl = gu.DeviceLayer(L, seed)
     x = synth.hidden(M, L.H, seed)
@@ -27,16 +28,15 @@ def _run(L, M, seed=0, sample=None):
     out, ws = dl.forward(x, ids, w)
     st, _ = moe.moe_w4a16_get_device_status(ws.buf)
     assert st == moe.MOE_OK, moe.moe_status_string(st)
-    got = gu.bf16_dev_to_f64(out)
-    rows = None if sample is None else gu.sample_rows(M, sample)
-    ref = dl.oracle(x, ids, w, rows)
-    return gu.parity(got if rows is None else got[rows], ref, f"E{L.E} H{L.H} I{L.I} k{L.k} M{M}")
+    what = f"E{L.E} H{L.H} I{L.I} k{L.k} M{M}"
+    ref, _ = gu.check_stages(dl, x, ids, w, ws.buf, np.arange(M * L.k), what)
+    return gu.parity(gu.bf16_dev_to_f64(out), ref["out"], what)
 
 
 def test_e1024_round_robin(gpu):
     import quantized_moe_expert_align_gb300 as moe
     L = synth.Layer(1024, 256, 128, 8)
-    _run(L, 2048, sample=48)
+    _run(L, 2048)
     assert moe.moe_w4a16_get_diag()["token_tile"] == 32
 
 

@@ -5,8 +5,10 @@ owns every device allocation, a decode loop where cudaMalloc would
 synchronise the device): instead of a caller-provided workspace it uses one
 static device array inside the library.  Here it is called through the C ABI
 twice in a row and must match the regular entry point, moe_w4a16_forward,
-within the parity tolerance of the other GPU tests; a size whose workspace
-exceeds the static array must be rejected before any launch.
+bit for bit: both run the same kernels on the same sizes, and the forward is
+deterministic (split tiles are reduced in a fixed order), so any difference
+would come from the static scratch itself.  A size whose workspace exceeds
+the static array must be rejected before any launch.
 
 The file name makes pytest collect it last, so a run that stops at the first
 failure has already run every other test; it also passes on its own.
@@ -27,7 +29,7 @@ def _static_matches_regular(dl, wl, M):
     x = synth.hidden(M, L.H, seed=3)
     ids, w = synth.routing(M, L, seed=3, zipf_s=wl.zipf_s)
     ref, _ = dl.forward(x, ids, w)
-    ref = gu.bf16_dev_to_f64(ref)
+    torch.cuda.synchronize()
     xd = gu.to_dev(x.view(np.int16)).view(torch.bfloat16)
     idd, wd = gu.to_dev(ids), gu.to_dev(w)
     for _ in range(2):
@@ -36,7 +38,9 @@ def _static_matches_regular(dl, wl, M):
                                           out, M, L.k, L.E, L.H, L.I)
         assert st == moe.MOE_OK, moe.moe_status_string(st)
         torch.cuda.synchronize()
-        gu.parity(gu.bf16_dev_to_f64(out), ref, f"static scratch {wl.name} M={M}")
+        same = out.view(torch.int16) == ref.view(torch.int16)
+        assert bool(same.all()), (f"static scratch {wl.name} M={M}: "
+                                  f"{int((~same).sum())} outputs differ from moe_w4a16_forward")
 
 
 def test_static_toy(toy_layer):
