@@ -3,10 +3,15 @@
 
 One step = one forward call per batch size of the workload (default: the
 decode sweep M in {1, 9, 90} of an E=384, H=7168, I=2048, top-8, INT4 g32
-layer), inputs already resident in HBM, L2 flushed before every step.
+layer), inputs already resident in HBM, L2 flushed before every call.  The
+headline value is that workload's tokens/s; the same run also times the rest
+of the metric's M range (the plateau M = 256-1024, the Zipf prefill M = 4096
+and 16384, the second layer shape E=128 M = 1-2048) the same way and reports
+each under ``other_workloads``.
 
   python bench.py [--gpus N] [--steps K] [--warmup W]
                   [--config decode|plateau|prefill|second|toy|e256|group128]
+                  [--extra plateau,prefill,second|none]
                   [--impl ours|reference]
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the plain CPU
@@ -267,117 +272,220 @@ def reference_arm(args, wl):
     return 0
 
 
+def layer_rows(wl, batches, call_ms, kernel_ms, hbm_peak, tf_peak):
+    """Per batch size: µs/call, tokens/s, active experts and the fraction of
+    roofline = max(touched experts' weight bytes / HBM copy rate,
+    6·M·k·H·I / dense fp16 peak) over the measured time."""
+    L = wl.layer
+    b13, b2 = expert_bytes(L)
+    rows = []
+    for M in wl.Ms:
+        active = int(np.unique(batches[M][1]).size)
+        roof_bytes = active * (b13 + b2)
+        flops = 6.0 * M * L.k * L.H * L.I
+        t_hbm = roof_bytes / (hbm_peak * 1e9)
+        t_tc = flops / (tf_peak * 1e12)
+        t_roof_ms = 1e3 * max(t_hbm, t_tc)
+        k_ms = kernel_ms[M]
+        rows.append({
+            "M": M, "active_experts": active,
+            "us_per_call": round(1e3 * call_ms[M], 2),
+            "tokens_per_s": round(M / (call_ms[M] / 1e3), 1),
+            "bound": "hbm" if t_hbm >= t_tc else "tensor",
+            "roofline_bytes": roof_bytes, "roofline_flops": flops,
+            "roofline_us": round(1e3 * t_roof_ms, 2),
+            "frac_of_roofline": round(t_roof_ms / call_ms[M], 4),
+            "kernel_ms": {n: round(float(v), 5) for n, v in zip(KERNELS, k_ms)},
+            "us_per_call_profiled": round(1e3 * float(k_ms.sum()), 2),
+            "pages_ms_rtx_pro_6000": PAGES_MS.get(M) if L.E == 384 else None,
+        })
+    return rows
+
+
+class Bench:
+    """The library loaded on this rank's GPU, plus what every workload's
+    timing shares: the stream, an L2-flush buffer and prepacked layers."""
+
+    def __init__(self, local):
+        import torch
+        import quantized_moe_expert_align_gb300 as moe
+        from quantized_moe_expert_align_gb300 import build as lib_build
+        self.torch, self.moe = torch, moe
+        lib_build.build()
+        moe.load()
+        self.stream = torch.cuda.current_stream()
+        l2 = torch.cuda.get_device_properties(local).L2_cache_size
+        self.flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
+        self.layers = {}
+
+    def dev(self, a):
+        return self.torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    def layer(self, L):
+        """(host canonical weights, prepacked w13, prepacked w2) of layer L."""
+        if L not in self.layers:
+            moe, torch = self.moe, self.torch
+            host_w = synth.layer_weights(L, 0)
+            q, s = self.dev(host_w[0]), self.dev(host_w[1].view(np.int16))
+            p13 = moe.prepack(moe.MOE_PACK_W13, q, s)
+            del q, s
+            q, s = self.dev(host_w[2]), self.dev(host_w[3].view(np.int16))
+            p2 = moe.prepack(moe.MOE_PACK_W2, q, s)
+            del q, s
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+            self.layers[L] = (host_w, p13, p2)
+        return self.layers[L]
+
+    def device_batches(self, wl, batches):
+        torch, L = self.torch, wl.layer
+        out = {}
+        for M, (x, ids, w) in batches.items():
+            out[M] = (self.dev(x.view(np.int16)).view(torch.bfloat16), self.dev(ids), self.dev(w),
+                      torch.empty((M, L.H), dtype=torch.bfloat16, device="cuda"))
+        return out
+
+    def caller(self, wl, devb, ws):
+        moe, L = self.moe, wl.layer
+        _, p13, p2 = self.layer(L)
+
+        def call(M):
+            x, ids, w, out = devb[M]
+            st = moe.moe_w4a16_forward(x, ids, w, p13, p2, out, M, L.k, L.E, L.H, L.I,
+                                       ws.buf, self.stream)
+            if st != moe.MOE_OK:
+                raise moe.MoeError(st, "moe_w4a16_forward")
+        return call
+
+    def timed(self, fn, Ms, steps):
+        """Per M, the device time (ms) of each of ``steps`` calls fn(M), CUDA
+        events on the launching stream around each call, L2 flushed (a
+        write of 2x L2) before every call, outside the events."""
+        torch = self.torch
+        ev = {M: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(steps)] for M in Ms}
+        for i in range(steps):
+            for M in Ms:
+                self.flush.zero_()
+                ev[M][i][0].record(self.stream)
+                fn(M)
+                ev[M][i][1].record(self.stream)
+        torch.cuda.synchronize()
+        return {M: [a.elapsed_time(b) for a, b in ev[M]] for M in Ms}
+
+    def kernel_times(self, wl, devb, ws, reps):
+        """Per M: mean ms of each library kernel (events between kernels,
+        moe_w4a16_forward_profiled), L2 flushed before every call."""
+        torch, moe, L = self.torch, self.moe, wl.layer
+        _, p13, p2 = self.layer(L)
+        per = {M: np.zeros(5) for M in wl.Ms}
+        for _ in range(reps):
+            for M in wl.Ms:
+                x, ids, w, out = devb[M]
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+                self.flush.zero_()
+                st = moe.moe_w4a16_forward_profiled(x, ids, w, p13, p2, out, M, L.k, L.E, L.H,
+                                                    L.I, ws.buf, evs, self.stream)
+                if st != moe.MOE_OK:
+                    raise moe.MoeError(st, "moe_w4a16_forward_profiled")
+                torch.cuda.synchronize()
+                per[M] += np.array([evs[i].elapsed_time(evs[i + 1]) for i in range(5)])
+        return {M: per[M] / reps for M in wl.Ms}
+
+    def check_status(self, ws, what):
+        moe = self.moe
+        st, detail = moe.moe_w4a16_get_device_status(ws.buf)
+        if st != moe.MOE_OK:
+            raise moe.MoeError(st, f"{what}: device status (detail {detail})")
+
+
+def extra_sweep(bench, wl, args, local, hbm_peak, tf_peak):
+    """One more workload of the metric's M range, timed like the headline
+    sweep (per call, L2 flushed before each), with its own clock record."""
+    torch, moe, L = bench.torch, bench.moe, wl.layer
+    batches = make_batches(wl)
+    devb = bench.device_batches(wl, batches)
+    ws = moe.Workspace(max(wl.Ms), L.k, L.E, L.H, L.I, "cuda")
+    call = bench.caller(wl, devb, ws)
+    for M in wl.Ms:
+        call(M)
+    bench.check_status(ws, wl.name)
+    for _ in range(args.warmup):
+        for M in wl.Ms:
+            call(M)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    ms = bench.timed(call, wl.Ms, args.steps)
+    clocks = sampler.stop()
+    call_ms = {M: float(np.mean(v)) for M, v in ms.items()}
+    kernel_ms = bench.kernel_times(wl, devb, ws, max(3, min(args.steps, 10)))
+    bench.check_status(ws, wl.name)
+    rows = layer_rows(wl, batches, call_ms, kernel_ms, hbm_peak, tf_peak)
+    del devb, ws
+    torch.cuda.empty_cache()
+    return {"workload": wl.name, "E": L.E, "H": L.H, "I": L.I, "k": L.k, "group": L.group,
+            "routing": "zipf(1.1)-biased" if wl.zipf_s else "uniform",
+            "timed_calls_per_M": args.steps, "clocks": clocks, "rows": rows}
+
+
 def our_arm(args, wl):
     import torch
     import torch.distributed as dist
-
-    import quantized_moe_expert_align_gb300 as moe
-    from quantized_moe_expert_align_gb300 import build as lib_build
 
     world, rank, local = dist_setup()
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
-    lib_build.build()
-    moe.load()
+    bench = Bench(local)
+    moe = bench.moe
     L = wl.layer
     hbm_peak, tf_peak, peak_kind = peaks()
-
-    # weights: canonical on the host (the oracle's copy), prepacked on the GPU
-    host_w = synth.layer_weights(L, 0)
-    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    q = dev(host_w[0])
-    s = dev(host_w[1].view(np.int16))
-    p13 = moe.prepack(moe.MOE_PACK_W13, q, s)
-    del q, s
-    q = dev(host_w[2])
-    s = dev(host_w[3].view(np.int16))
-    p2 = moe.prepack(moe.MOE_PACK_W2, q, s)
-    del q, s
-    torch.cuda.synchronize()
-    torch.cuda.empty_cache()
+    host_w, p13, p2 = bench.layer(L)
 
     batches = make_batches(wl)
-    Mmax = max(wl.Ms)
-    ws = moe.Workspace(Mmax, L.k, L.E, L.H, L.I, "cuda")
-    devb = {}
-    for M, (x, ids, w) in batches.items():
-        devb[M] = (dev(x.view(np.int16)).view(torch.bfloat16), dev(ids), dev(w),
-                   torch.empty((M, L.H), dtype=torch.bfloat16, device="cuda"))
-    stream = torch.cuda.current_stream()
-    l2 = torch.cuda.get_device_properties(local).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
-
-    def call(M):
-        x, ids, w, out = devb[M]
-        st = moe.moe_w4a16_forward(x, ids, w, p13, p2, out, M, L.k, L.E,
-                                   L.H, L.I, ws.buf, stream)
-        if st != moe.MOE_OK:
-            raise moe.MoeError(st, "moe_w4a16_forward")
-
-    def step():
-        for M in wl.Ms:
-            call(M)
+    ws = moe.Workspace(max(wl.Ms), L.k, L.E, L.H, L.I, "cuda")
+    devb = bench.device_batches(wl, batches)
+    stream = bench.stream
+    flush = bench.flush
+    call = bench.caller(wl, devb, ws)
+    dev = bench.dev
 
     # correctness gate before timing (device status of the last call)
-    step()
-    st, detail = moe.moe_w4a16_get_device_status(ws.buf)
-    if st != moe.MOE_OK:
-        raise moe.MoeError(st, f"device status (detail {detail})")
+    for M in wl.Ms:
+        call(M)
+    bench.check_status(ws, "first forward")
     for _ in range(args.warmup):
-        step()
+        for M in wl.Ms:
+            call(M)
     torch.cuda.synchronize()
 
-    # ---- timed region: K steps, device time per step, L2 flushed between ----
-    # Events also mark each call inside a step (the first kernel of a call
-    # waits for the previous call anyway, so they do not change the timing).
-    nM = len(wl.Ms)
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nM + 1)] for _ in range(args.steps)]
+    # ---- timed region: K steps of one call per M; device time per call,
+    # L2 flushed before every call (outside the events) ----
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.zero_()
-        marks[i][0].record(stream)
-        for j, M in enumerate(wl.Ms):
-            call(M)
-            marks[i][j + 1].record(stream)
-    torch.cuda.synchronize()
+    ms = bench.timed(call, wl.Ms, args.steps)
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    step_ms = [m[0].elapsed_time(m[nM]) for m in marks]
-    call_ms = {M: float(np.mean([m[j].elapsed_time(m[j + 1]) for m in marks]))
-               for j, M in enumerate(wl.Ms)}
-    total_ms = max_over_ranks(sum(step_ms), "cuda")
+    call_ms = {M: float(np.mean(v)) for M, v in ms.items()}
+    total_ms = max_over_ranks(sum(sum(v) for v in ms.values()), "cuda")
     tokens_per_step = sum(wl.Ms)
     value = job_value(tokens_per_step, args.steps, world, total_ms)
     launches_per_step = 0
-    for M in wl.Ms:   # kernels per call differ with M (small batches fuse two)
+    for M in wl.Ms:   # kernels per call differ with M (the router's, the large alignment)
         call(M)
         launches_per_step += moe.moe_w4a16_get_diag()["kernels_launched"]
     torch.cuda.synchronize()
     gpu_launches = launches_per_step * args.steps
 
     # ---- per-kernel durations (events between the library's kernels) ----
-    prof_steps = max(3, min(args.steps, 10))
-    per_kernel = {M: np.zeros(5) for M in wl.Ms}
-    for _ in range(prof_steps):
-        for M in wl.Ms:
-            x, ids, w, out = devb[M]
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-            flush.zero_()
-            st = moe.moe_w4a16_forward_profiled(x, ids, w, p13, p2, out, M,
-                                                L.k, L.E, L.H, L.I, ws.buf, evs, stream)
-            if st != moe.MOE_OK:
-                raise moe.MoeError(st, "moe_w4a16_forward_profiled")
-            torch.cuda.synchronize()
-            per_kernel[M] += np.array([evs[i].elapsed_time(evs[i + 1]) for i in range(5)])
-    for M in wl.Ms:
-        per_kernel[M] /= prof_steps
+    per_kernel = bench.kernel_times(wl, devb, ws, max(3, min(args.steps, 10)))
 
     # ---- router front-end: logits -> ids, weights and alignment alone
     # (moe_route_align), and the whole layer from logits
@@ -427,9 +535,7 @@ def our_arm(args, wl):
         torch.cuda.synchronize()
         t_route = ev[0].elapsed_time(ev[1]) / reps
         t_layer = float(np.mean([ev[2 + 2 * r].elapsed_time(ev[3 + 2 * r]) for r in range(reps)]))
-        st, detail = moe.moe_w4a16_get_device_status(ws.buf)
-        if st != moe.MOE_OK:
-            raise moe.MoeError(st, f"routed forward device status (detail {detail})")
+        bench.check_status(ws, "routed forward")
         if not torch.equal(r_ids, ids):
             raise RuntimeError(f"routed ids differ from the batch's routing at M={M}")
         nbytes = M * L.E * 4 + M * L.k * 8
@@ -470,34 +576,19 @@ def our_arm(args, wl):
         graph_us[M] = round(1e3 * float(np.mean([ev[2 * r].elapsed_time(ev[2 * r + 1])
                                                    for r in range(reps)])), 2)
         del graph
-    st, detail = moe.moe_w4a16_get_device_status(ws.buf)
-    if st != moe.MOE_OK:
-        raise moe.MoeError(st, f"graph replay device status (detail {detail})")
+    bench.check_status(ws, "graph replay")
 
     # roofline: the gate+up GEMM streams the touched experts' w13 codes+scales
     b13, b2 = expert_bytes(L)
-    sweep = []
+    sweep = layer_rows(wl, batches, call_ms, per_kernel, hbm_peak, tf_peak)
     gemm1_bytes = gemm1_ms = 0.0
-    for M in wl.Ms:
-        active = int(np.unique(batches[M][1]).size)
-        k_ms = per_kernel[M]
-        gemm1_bytes += active * b13
-        gemm1_ms += float(k_ms[2])
-        roof_bytes = active * (b13 + b2)
-        flops = 6.0 * M * L.k * L.H * L.I
-        t_roof_ms = 1e3 * max(roof_bytes / (hbm_peak * 1e9), flops / (tf_peak * 1e12))
-        sweep.append({
-            "M": M, "active_experts": active,
-            "us_per_call": round(1e3 * call_ms[M], 2), "tokens_per_s": round(M / (call_ms[M] / 1e3), 1),
-            "frac_of_roofline": round(t_roof_ms / call_ms[M], 4),
-            "kernel_ms": {n: round(float(v), 5) for n, v in zip(KERNELS, k_ms)},
-            "us_per_call_profiled": round(1e3 * float(k_ms.sum()), 2),
-            "roofline_bytes": roof_bytes, "roofline_us": round(1e3 * t_roof_ms, 2),
-            "frac_of_roofline_profiled": round(t_roof_ms / float(k_ms.sum()), 4),
-            "pages_ms_rtx_pro_6000": PAGES_MS.get(M) if L.E == 384 else None,
-            "router": router[M],
-            "us_per_call_graph": graph_us[M],
-        })
+    for row in sweep:
+        M = row["M"]
+        gemm1_bytes += row["active_experts"] * b13
+        gemm1_ms += float(per_kernel[M][2])
+        row["router"] = router[M]
+        row["us_per_call_graph"] = graph_us[M]
+        row["frac_of_roofline_profiled"] = round(row["roofline_us"] / row["us_per_call_profiled"], 4)
     achieved = gemm1_bytes / (gemm1_ms / 1e3) / 1e9
     traffic = None
     tc = TRAFFIC_CAPTURE
@@ -506,10 +597,10 @@ def our_arm(args, wl):
         traffic = float(np.mean([tc["bytes_per_launch"][M] for M in wl.Ms]))
 
     # ---- end to end through the C ABI: pinned host inputs and output.  A
-    # step's inputs (hidden, ids, weights) sit packed in one pinned buffer and
+    # call's inputs (hidden, ids, weights) sit packed in one pinned buffer and
     # go over in one copy to one device buffer whose slices are the call's
-    # arguments; the output comes back in one copy. ----
-    e2e = None
+    # arguments; the output comes back in one copy.  Timed per call, L2
+    # flushed before each, like the device-resident steps. ----
     host = {}
     h2d = d2h = 0
 
@@ -558,18 +649,11 @@ def our_arm(args, wl):
     for M in wl.Ms:
         if not torch.equal(host[M][5], ref_out[M].cpu()):
             raise RuntimeError(f"end-to-end output differs at M={M}")
-    e_st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    e_en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush.zero_()
-        e_st[i].record(stream)
-        for M in wl.Ms:
-            e2e_call(M)
-        e_en[i].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(e_st, e_en)), "cuda")
+    e_ms = bench.timed(e2e_call, wl.Ms, args.steps)
+    e2e_ms = max_over_ranks(sum(sum(v) for v in e_ms.values()), "cuda")
     e2e = {"value": job_value(tokens_per_step, args.steps, world, e2e_ms), "unit": "tokens/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "timing": "per call, L2 flushed before each; copies inside the events"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -579,6 +663,17 @@ def our_arm(args, wl):
         tok, secs = run_oracle(wl, host_w, sample)
         cpu = {"value": tok / secs, "unit": "tokens/s", "cores": oracle.num_threads(),
                "kind": "oracle", "sample": describe_sample(sample, wl)}
+
+    # ---- the rest of the metric's M range: the other workloads, each timed
+    # the same way (the headline value stays the decode sweep) ----
+    del devb, host
+    torch.cuda.empty_cache()
+    extras = []
+    for name in args.extra:
+        xwl = CONFIGS[name]
+        if xwl is wl:
+            continue
+        extras.append(extra_sweep(bench, xwl, args, local, hbm_peak, tf_peak))
 
     pages = [PAGES_MS.get(M) for M in wl.Ms]
     vs = None
@@ -595,7 +690,7 @@ def our_arm(args, wl):
             "config": {"workload": wl.name, "Ms": list(wl.Ms), "E": L.E, "H": L.H, "I": L.I,
                        "k": L.k, "group": L.group,
                        "routing": "zipf(1.1)-biased" if wl.zipf_s else "uniform",
-                       "l2": "flushed before every step (write of 2x L2)",
+                       "l2": "flushed before every call (write of 2x L2, outside the events)",
                        "parallelism": f"replicas x{world}",
                        "vs_baseline_ref": "pages' sweep on one RTX PRO 6000 (sm_120): context"},
             "clocks": clocks, "e2e": e2e, "gpu_launches": gpu_launches,
@@ -606,7 +701,7 @@ def our_arm(args, wl):
                          "traffic_source": tc["profile"] if traffic is not None else None,
                          "algorithmic_bytes_per_unit": b13,
                          "unit_of_work": "active expert (w13 codes + scales)"},
-            "cpu_baseline": cpu, "sweep": sweep,
+            "cpu_baseline": cpu, "sweep": sweep, "other_workloads": extras,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -624,7 +719,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-slots", type=int, default=800,
                     help="slots the CPU-baseline oracle sample covers")
+    ap.add_argument("--extra", default=None,
+                    help="comma-separated further workloads timed in the same run "
+                         "(default with the decode sweep: plateau,prefill,second; "
+                         "'none' for none)")
     args = ap.parse_args()
+    if args.extra is None:
+        args.extra = "plateau,prefill,second" if args.config == "decode" else "none"
+    args.extra = [] if args.extra == "none" else [e for e in args.extra.split(",") if e]
+    for e in args.extra:
+        if e not in CONFIGS:
+            ap.error(f"--extra: unknown workload {e!r}")
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     wl = CONFIGS[args.config]
