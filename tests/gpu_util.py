@@ -103,7 +103,16 @@ def sample_rows(M: int, count: int, seed: int = 1) -> np.ndarray:
 # workspace (act = silu(gate)*up as an fp16 hi + lo pair, y the down
 # projection, both per expert-sorted row) against the oracle's, slot by slot.
 # ---------------------------------------------------------------------------
-STAGE_ATOL = 1e-3   # |gpu - oracle| <= STAGE_ATOL + STAGE_RTOL * |oracle| for act and y
+# |gpu - oracle| <= STAGE_ATOL + STAGE_RTOL * |oracle| for act and y.  Each
+# slot's y enters the output multiplied by its routing weight (the k weights
+# sum to 1), so a y within half the layer's absolute tolerance keeps its
+# share of the output error inside the layer's bound; the relative part is
+# ten times tighter than the layer's.  Measured: the largest absolute y error
+# over the whole suite is 1.1e-3 (E=384, Zipf M = 4096, at y ~ 0.01: the
+# tensor core's fp32 accumulation over 2 x 2048 K steps of products up to
+# ~40, plus the fast exp/divide of SiLU inside act); a wrong row, chunk,
+# scale or slot gives errors of order |y| ~ 25.
+STAGE_ATOL = 5e-3
 STAGE_RTOL = 1e-3
 
 
