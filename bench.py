@@ -45,6 +45,7 @@ CONFIGS = {"decode": synth.DECODE, "plateau": synth.PLATEAU, "prefill": synth.PR
 # The pages' sweep on one RTX PRO 6000 (sm_120), context only: ms per call.
 PAGES_MS = {1: 0.151, 9: 1.18, 90: 5.19, 256: 7.02, 512: 7.01, 1024: 7.02}
 KERNELS = ["align", "gather", "gemm_gate_up", "gemm_down", "combine"]
+FUSED_KERNEL = "decode_fused"   # small batches: the whole layer in one kernel
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum, one ncu pass,
 # caches flushed by ncu before each launch) of the gate+up GEMM launches of
@@ -53,13 +54,15 @@ KERNELS = ["align", "gather", "gemm_gate_up", "gemm_down", "combine"]
 # comments and blank lines removed).  For any other source the figure no
 # longer describes the kernel and the bench reports traffic as null.
 TRAFFIC_CAPTURE = {
+    "kernel": "gemm_gate_up",
     "sources_sha256": "901e484ff0c5ecfa6fed37872673523693baa9d8ed0bb1e84fc9822c2e079ec4",
     "workload": "decode_e384_h7168_i2048_top8",
     "bytes_per_launch": {1: 132315904 + 2819072, 9: 1091143424 + 558592,
                          90: 5559521792 + 1895680},
     "profile": "profiles/dram_gemm_gate_up_decode_e384_m1_9_90.md",
 }
-KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "sm100.cuh", "moe_internal.h", "device_common.cuh"]
+KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "tc_common.cuh", "sm100.cuh", "moe_internal.h",
+                  "device_common.cuh", "decode.cu", "decode.h"]
 
 
 def code_only(text):
@@ -286,7 +289,8 @@ def layer_rows(wl, batches, call_ms, kernel_ms, hbm_peak, tf_peak):
         t_hbm = roof_bytes / (hbm_peak * 1e9)
         t_tc = flops / (tf_peak * 1e12)
         t_roof_ms = 1e3 * max(t_hbm, t_tc)
-        k_ms = kernel_ms[M]
+        k_ms, fused = kernel_ms[M]
+        names = [FUSED_KERNEL] if fused else KERNELS
         rows.append({
             "M": M, "active_experts": active,
             "us_per_call": round(1e3 * call_ms[M], 2),
@@ -295,7 +299,7 @@ def layer_rows(wl, batches, call_ms, kernel_ms, hbm_peak, tf_peak):
             "roofline_bytes": roof_bytes, "roofline_flops": flops,
             "roofline_us": round(1e3 * t_roof_ms, 2),
             "frac_of_roofline": round(t_roof_ms / call_ms[M], 4),
-            "kernel_ms": {n: round(float(v), 5) for n, v in zip(KERNELS, k_ms)},
+            "kernel_ms": {n: round(float(v), 5) for n, v in zip(names, k_ms)},
             "us_per_call_profiled": round(1e3 * float(k_ms.sum()), 2),
             "pages_ms_rtx_pro_6000": PAGES_MS.get(M) if L.E == 384 else None,
         })
@@ -374,11 +378,14 @@ class Bench:
         return {M: [a.elapsed_time(b) for a, b in ev[M]] for M in Ms}
 
     def kernel_times(self, wl, devb, ws, reps):
-        """Per M: mean ms of each library kernel (events between kernels,
-        moe_w4a16_forward_profiled), L2 flushed before every call."""
+        """Per M: (mean ms of each library kernel, whether the call ran as the
+        single small-batch kernel) -- events between kernels
+        (moe_w4a16_forward_profiled), L2 flushed before every call.  The
+        single kernel's time is the first entry."""
         torch, moe, L = self.torch, self.moe, wl.layer
         _, p13, p2 = self.layer(L)
         per = {M: np.zeros(5) for M in wl.Ms}
+        fused = {}
         for _ in range(reps):
             for M in wl.Ms:
                 x, ids, w, out = devb[M]
@@ -388,9 +395,10 @@ class Bench:
                                                     L.I, ws.buf, evs, self.stream)
                 if st != moe.MOE_OK:
                     raise moe.MoeError(st, "moe_w4a16_forward_profiled")
+                fused[M] = moe.moe_w4a16_get_diag()["kernels_launched"] == 1
                 torch.cuda.synchronize()
                 per[M] += np.array([evs[i].elapsed_time(evs[i + 1]) for i in range(5)])
-        return {M: per[M] / reps for M in wl.Ms}
+        return {M: (per[M][:1] if fused[M] else per[M]) / reps for M in wl.Ms}, fused
 
     def check_status(self, ws, what):
         moe = self.moe
@@ -420,9 +428,10 @@ def extra_sweep(bench, wl, args, local, hbm_peak, tf_peak):
     ms = bench.timed(call, wl.Ms, args.steps)
     clocks = sampler.stop()
     call_ms = {M: float(np.mean(v)) for M, v in ms.items()}
-    kernel_ms = bench.kernel_times(wl, devb, ws, max(3, min(args.steps, 10)))
+    k_ms, fused = bench.kernel_times(wl, devb, ws, max(3, min(args.steps, 10)))
     bench.check_status(ws, wl.name)
-    rows = layer_rows(wl, batches, call_ms, kernel_ms, hbm_peak, tf_peak)
+    rows = layer_rows(wl, batches, call_ms, {M: (k_ms[M], fused[M]) for M in wl.Ms}, hbm_peak,
+                      tf_peak)
     del devb, ws
     torch.cuda.empty_cache()
     return {"workload": wl.name, "E": L.E, "H": L.H, "I": L.I, "k": L.k, "group": L.group,
@@ -485,7 +494,7 @@ def our_arm(args, wl):
     gpu_launches = launches_per_step * args.steps
 
     # ---- per-kernel durations (events between the library's kernels) ----
-    per_kernel = bench.kernel_times(wl, devb, ws, max(3, min(args.steps, 10)))
+    per_kernel, fused = bench.kernel_times(wl, devb, ws, max(3, min(args.steps, 10)))
 
     # ---- router front-end: logits -> ids, weights and alignment alone
     # (moe_route_align), and the whole layer from logits
@@ -578,23 +587,36 @@ def our_arm(args, wl):
         del graph
     bench.check_status(ws, "graph replay")
 
-    # roofline: the gate+up GEMM streams the touched experts' w13 codes+scales
+    # roofline of the dominant kernel (the most device time over the sweep):
+    # its algorithmic bytes -- the touched experts' codes + scales it streams
+    # (w13 for the gate+up GEMM, w2 for the down GEMM, both for the single
+    # small-batch kernel) -- over its mean launch duration
     b13, b2 = expert_bytes(L)
-    sweep = layer_rows(wl, batches, call_ms, per_kernel, hbm_peak, tf_peak)
-    gemm1_bytes = gemm1_ms = 0.0
+    sweep = layer_rows(wl, batches, call_ms, {M: (per_kernel[M], fused[M]) for M in wl.Ms},
+                       hbm_peak, tf_peak)
+    per_name = {}
     for row in sweep:
         M = row["M"]
-        gemm1_bytes += row["active_experts"] * b13
-        gemm1_ms += float(per_kernel[M][2])
+        active = row["active_experts"]
+        unit_bytes = {FUSED_KERNEL: b13 + b2, "gemm_gate_up": b13, "gemm_down": b2}
+        for name, ms_ in row["kernel_ms"].items():
+            if name in unit_bytes:
+                acc = per_name.setdefault(name, [0.0, 0.0, 0, unit_bytes[name]])
+                acc[0] += active * unit_bytes[name]
+                acc[1] += ms_
+                acc[2] += 1
         row["router"] = router[M]
         row["us_per_call_graph"] = graph_us[M]
         row["frac_of_roofline_profiled"] = round(row["roofline_us"] / row["us_per_call_profiled"], 4)
-    achieved = gemm1_bytes / (gemm1_ms / 1e3) / 1e9
+    dom = max(per_name, key=lambda nm: per_name[nm][1])
+    dom_bytes, dom_ms, dom_launches, dom_unit = per_name[dom]
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     traffic = None
     tc = TRAFFIC_CAPTURE
+    dom_Ms = [row["M"] for row in sweep if dom in row["kernel_ms"]]
     if (tc["sources_sha256"] == kernel_sources_sha256() and tc["workload"] == wl.name
-            and all(M in tc["bytes_per_launch"] for M in wl.Ms)):
-        traffic = float(np.mean([tc["bytes_per_launch"][M] for M in wl.Ms]))
+            and tc["kernel"] == dom and all(M in tc["bytes_per_launch"] for M in dom_Ms)):
+        traffic = float(np.mean([tc["bytes_per_launch"][M] for M in dom_Ms]))
 
     # ---- end to end through the C ABI: pinned host inputs and output.  A
     # call's inputs (hidden, ids, weights) sit packed in one pinned buffer and
@@ -694,13 +716,14 @@ def our_arm(args, wl):
                        "parallelism": f"replicas x{world}",
                        "vs_baseline_ref": "pages' sweep on one RTX PRO 6000 (sm_120): context"},
             "clocks": clocks, "e2e": e2e, "gpu_launches": gpu_launches,
-            "roofline": {"bound": "hbm", "kernel": "gemm_gate_up", "achieved": achieved,
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved,
                          "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                          "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic,
-                         "algorithmic_bytes_per_launch": gemm1_bytes / len(wl.Ms),
+                         "algorithmic_bytes_per_launch": dom_bytes / dom_launches,
+                         "launches_averaged": {"Ms": dom_Ms, "count": dom_launches},
                          "traffic_source": tc["profile"] if traffic is not None else None,
-                         "algorithmic_bytes_per_unit": b13,
-                         "unit_of_work": "active expert (w13 codes + scales)"},
+                         "algorithmic_bytes_per_unit": dom_unit,
+                         "unit_of_work": "active expert (codes + scales the kernel streams)"},
             "cpu_baseline": cpu, "sweep": sweep, "other_workloads": extras,
         }
         print(json.dumps(line), flush=True)

@@ -191,6 +191,13 @@ size_t moe_w4a16_workspace_size(int M, int k, int E, int H, int I);
  * Numerics: weights dequantised exactly to fp16, hidden converted to fp16
  * (values beyond fp16 range set MOE_ERR_DEVICE_FP16_RANGE), fp32
  * accumulation, the activation passed to the down GEMM as an fp16 hi+lo pair.
+ * Kernels: batches of at most 128 slots (M*k) whose token tile is 16 rows
+ * run as one cooperative kernel of one CTA per SM (every CTA resident at
+ * once; the call fails with MOE_ERR_CUDA where the device cannot host
+ * that); larger ones as five kernels (alignment, hidden gather, gate+up
+ * GEMM, down GEMM, combine).  For testing, MOE_W4A16_DECODE_FUSED=0 (read
+ * once per process) sends small batches through the five kernels too.
+ * Either way the same results are written to `out` and to the workspace.
  */
 moe_status_t moe_w4a16_forward(const uint16_t *hidden, const int32_t *topk_ids,
                                const float *topk_w, const void *w13, const void *w2,
@@ -219,9 +226,12 @@ moe_status_t moe_w4a16_forward_routed(const uint16_t *hidden, const float *logit
  * n_events >= 6 cudaEvent_t handles (created by the caller, timing enabled):
  * events[i] is recorded right before kernel i and events[5] after the last;
  * kernel order: 0 align, 1 hidden gather, 2 gate+up GEMM, 3 down GEMM,
- * 4 combine.  Recording between kernels stops them from overlapping, so the
- * sum of the intervals can exceed the plain forward's time.  Returns
- * MOE_ERR_INVALID_ARG if events is NULL or n_events < 6.
+ * 4 combine.  When the call runs as the single small-batch kernel,
+ * events[0] is recorded right before it and events[1..5] right after it
+ * (moe_w4a16_get_diag then reports one kernel).  Recording between kernels
+ * stops them from overlapping, so the sum of the intervals can exceed the
+ * plain forward's time.  Returns MOE_ERR_INVALID_ARG if events is NULL or
+ * n_events < 6.
  */
 moe_status_t moe_w4a16_forward_profiled(const uint16_t *hidden, const int32_t *topk_ids,
                                         const float *topk_w, const void *w13, const void *w2,
@@ -277,7 +287,10 @@ moe_status_t moe_w4a16_forward_static(const uint16_t *hidden, const int32_t *top
  * Wait for `stream`, then return the status word the device recorded in
  * `workspace` during the most recent align/forward call on it (MOE_OK if
  * nothing went wrong).  `detail` (may be NULL) receives a code-specific
- * value: the offending id, or the kernel that gave up.
+ * value: the offending id, or the role whose bounded wait gave up (1 a
+ * producer, 2/3 an MMA issuer, 4/5 a dequantisation warp, 6 the epilogue,
+ * 7 the single small-batch kernel's wait for activation rows that another
+ * CTA writes).
  */
 moe_status_t moe_w4a16_get_device_status(const void *workspace,
                                          moe_stream_t stream, int32_t *detail);

@@ -4,6 +4,7 @@
 #include <cstdlib>
 #include <cstring>
 
+#include "decode.h"
 #include "elementwise.h"
 #include "gemm_tc.h"
 #include "moe_internal.h"
@@ -48,6 +49,20 @@ static int test_no_copies() {
     return v;
 }
 
+// Test switch, read once per process: MOE_W4A16_DECODE_FUSED=0 sends small
+// batches through the five-kernel path too.
+static bool decode_kernel_enabled() {
+    static const bool on = [] {
+        const char *v = std::getenv("MOE_W4A16_DECODE_FUSED");
+        return !(v && std::atoi(v) == 0);
+    }();
+    return on;
+}
+
+bool use_decode_kernel(int64_t n, int nt) {
+    return decode_kernel_enabled() && n > 0 && n <= kDecodeMaxSlots && nt == kDecodeTokenTile;
+}
+
 // The down GEMM's stage holds both halves (hi, lo) of its token rows, so a
 // 128-row tile leaves room for only two stages: it uses 64-row tiles there.
 int down_token_tile(int nt) {
@@ -76,6 +91,7 @@ FwdLayout fwd_layout(int M, int k, int E, int H, int I) {
     FwdLayout l;
     l.nt = pick_token_tile((int)n, E);
     l.nt2 = down_token_tile(l.nt);
+    l.fused = use_decode_kernel((int64_t)n, l.nt);
     l.max_tok_tiles = (int)(n / l.nt) + (n < (size_t)E ? (int)n : E) + 1;
     l.max_tok_tiles2 = (int)(n / l.nt2) + (n < (size_t)E ? (int)n : E) + 1;
     l.grid = kMaxGrid;
@@ -97,10 +113,13 @@ FwdLayout fwd_layout(int M, int k, int E, int H, int I) {
     l.tile_prefix2 = take((size_t)(E + 1) * 4);
     l.perm = take(n * 4);
     l.inv_perm = take(n * 4);
-    // one ticket per (tile, epilogue warp)
-    l.tickets = take(((size_t)l.max_tok_tiles * (2 * I / kTileRows) +
-                      (size_t)l.max_tok_tiles2 * (H / kTileRows)) * 4 * 4);
-    l.partials = take((size_t)l.grid * 2 * l.nt * kTileRows * 4);
+    // one ticket per (tile, epilogue warp); the single small-batch kernel
+    // also keeps its activation-ready flags and combine tickets there, and
+    // the partials of both GEMMs
+    l.tickets = l.fused ? take((size_t)decode_sync_ints(l.max_tok_tiles, H, I) * 4)
+                        : take(((size_t)l.max_tok_tiles * (2 * I / kTileRows) +
+                                (size_t)l.max_tok_tiles2 * (H / kTileRows)) * 4 * 4);
+    l.partials = take((size_t)(l.fused ? 2 : 1) * l.grid * 2 * l.nt * kTileRows * 4);
     l.xs = take(n * H * 2);
     l.act_hi = take(n * I * 2);
     l.act_lo = take(n * I * 2);
@@ -444,6 +463,69 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
         return MOE_ERR_CUDA;
 
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
+
+    if (L.fused) {
+        // The whole layer in one cooperative kernel; with logits the router
+        // runs first (after the status word is cleared), and the kernel then
+        // leaves the word alone.
+        DecodeArgs d = {};
+        d.hidden = hidden;
+        d.ids = ids;
+        d.topk_w = topk_w;
+        d.w13 = g1.w;
+        d.w2 = g2.w;
+        d.out = out;
+        d.M = M;
+        d.k = k;
+        d.E = E;
+        d.H = H;
+        d.I = I;
+        d.reset_status = logits ? 0 : 1;
+        d.ctrl = ctrl;
+        d.counts = counts;
+        d.offsets = offsets;
+        d.perm = perm;
+        d.inv_perm = inv_perm;
+        d.sync = tickets;
+        d.sync_ints = decode_sync_ints(L.max_tok_tiles, H, I);
+        d.partials = partials;
+        d.xs = xs;
+        d.act_hi = act_hi;
+        d.act_lo = act_lo;
+        d.y = y;
+        d.test_no_copies = test_no_copies();
+        bool routed = false;
+        if (logits) {
+            RouteArgs r = {logits, M, E, k, const_cast<int32_t *>(ids), const_cast<float *>(topk_w), ctrl};
+            if (cudaMemsetAsync(ctrl, 0, 4 * sizeof(int32_t), s) != cudaSuccess ||
+                launch_route(r, s) != cudaSuccess) {
+                cudaGetLastError();
+                return MOE_ERR_CUDA;
+            }
+            routed = true;
+        }
+        if (mark(0) != cudaSuccess || launch_decode(d, map_x, map_act, grid, s) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+        for (int i = 1; i < 6; ++i)
+            if (mark(i) != cudaSuccess) {
+                cudaGetLastError();
+                return MOE_ERR_CUDA;
+            }
+        g_diag.M = M;
+        g_diag.k = k;
+        g_diag.E = E;
+        g_diag.H = H;
+        g_diag.I = I;
+        g_diag.token_tile = L.nt;
+        g_diag.grid_gemm1 = grid;
+        g_diag.grid_gemm2 = grid;
+        g_diag.kernels_launched = 1 + (routed ? 1 : 0);
+        g_diag.workspace_bytes = (int64_t)L.total;
+        g_diag.calls += 1;
+        return MOE_OK;
+    }
     const bool pdl = (ev == nullptr);
     bool route_kernel = false;
     set_segments(al, ws, L.seg_counts, L.seg_base);

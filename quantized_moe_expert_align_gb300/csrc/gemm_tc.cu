@@ -45,12 +45,14 @@
 
 #include "device_common.cuh"
 #include "sm100.cuh"
+#include "tc_common.cuh"
 #include "gemm_tc.h"
 
 namespace moe {
 namespace {
 
 using namespace sm100;
+using namespace tc;
 
 constexpr int kEpiWarps = 4;
 // Warps: 4 epilogue, 4 per dequantisation warpgroup, one or two TMA
@@ -61,8 +63,6 @@ __host__ __device__ constexpr int threads_for(int dq_groups, int producers, int 
 constexpr int kMaxABufs = 6;                  // TMEM A buffers (64 columns each)
 constexpr int kACols = kChunkK / 2;           // 64 fp16 pairs per row per chunk
 constexpr uint32_t kTmemCols = 512;
-constexpr long long kWaitCycles = 1ll << 31;  // bounded waits give up after ~1-2 s
-constexpr uint32_t kSleepNs = 20000;          // longest sleep of one poll of a wait
 
 struct Smem {
     uint64_t full[kMaxStages];      // stage loaded (TMA transaction bytes)
@@ -79,58 +79,6 @@ struct Smem {
     int32_t tile_prefix[1025];
     int32_t offsets[1025];
 };
-
-// Bounded wait that also gives up as soon as another role has aborted.  The
-// limit is measured with the SM's own cycle counter, which never runs
-// backwards.
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Smem *sm, Ctrl *ctrl,
-                                         int who) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
-        if (*(volatile int *)&sm->abort) return false;
-        if (clock64() - t0 > kWaitCycles) {
-            atomicExch(&sm->abort, 1);
-            set_status(ctrl, MOE_ERR_DEVICE_TIMEOUT, who);
-            return false;
-        }
-    }
-}
-
-// All lanes of a warp wait; the warp goes on only if every lane saw the
-// phase complete, so later warp-wide (.sync.aligned) instructions stay
-// convergent even when an abort races with completion.
-__device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, Smem *sm, Ctrl *ctrl,
-                                              int who) {
-    const bool ok = wait_bar(bar, parity, sm, ctrl, who);
-    return __all_sync(0xffffffffu, ok);
-}
-
-// Bounded wait that ignores the abort flag (used while winding down).
-__device__ __forceinline__ bool wait_bar_final(uint64_t *bar, uint32_t parity) {
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity))
-        if (clock64() - t0 > kWaitCycles) return false;
-    return true;
-}
-
-// Stream-K partition of W chunk-units over G CTAs.
-__device__ __forceinline__ int64_t range_begin(int g, int64_t W, int G) {
-    return (int64_t)g * W / G;
-}
-__device__ __forceinline__ int unit_owner(int64_t u, int64_t W, int G) {
-    return (int)(((u + 1) * (int64_t)G - 1) / W);
-}
-// Number of CTAs whose (non-empty) ranges cover units [u0, u1].
-__device__ __forceinline__ int contributors(int64_t u0, int64_t u1, int64_t W, int G) {
-    int n = 0;
-    for (int g = unit_owner(u0, W, G);; g = unit_owner(range_begin(g + 1, W, G), W, G)) {
-        ++n;
-        if (range_begin(g + 1, W, G) > u1) break;
-    }
-    return n;
-}
 
 struct Tile {
     int e, rt, p0, rows;
@@ -157,71 +105,6 @@ __device__ __forceinline__ Tile decode_tile(const TcArgs &a, const Smem *sm, int
     t.p0 = sm->offsets[lo] + tt * NT;
     t.rows = min(NT, sm->offsets[lo + 1] - t.p0);
     return t;
-}
-
-// Dequantisation of one 32-bit code word: the 8 weights (q - 8) * scale,
-// exactly, as 4 fp16 pairs in element order (elements 2j, 2j+1 -> o[j]).
-// Element i's code sits at bit nibble_pos(i) = 6, 22, 10, 26, 14, 30, 18, 2
-// (the one at 30 wraps to bits 0-1), so that
-//  * w & 0x03C003C0 holds elements 0 and 1 at bits 6-9 of each half, and a
-//    rotation by 4 brings elements 2 and 3 there: OR-ing the exponent of 16
-//    makes the fp16 values 16 + q, and one fused multiply-add with the
-//    scale s and -24 s gives (16 + q) s - 24 s = (q - 8) s, rounded once
-//    from the exact value, which is itself an fp16 number (s has at most 8
-//    significant bits, q - 8 at most 4);
-//  * a rotation by 14 brings elements 4, 5 to bits 0-3 and 6, 7 to bits
-//    4-7 of each half: OR-ing the exponent of 1024 makes 1024 + q (or
-//    1024 + 16 q), minus 1032 (or times 1/16 minus 72) is q - 8 exactly,
-//    then a product with s.
-// The fused form needs -24 s in fp16 (|s| <= 65504/24); buffers with wider
-// or infinite scales use exact_pairs for elements 0-3 as well.  The two
-// ways split the work evenly between the integer and the fp16 pipes.
-__device__ __forceinline__ uint32_t rotr(uint32_t x, int n) { return __funnelshift_r(x, x, n); }
-
-__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
-
-// (1024 + q) and (1024 + 16 q) at bits 0-3 / 4-7 of each half of x -> 2 pairs
-__device__ __forceinline__ void exact_pairs(uint32_t x, __half2 s2, uint32_t &lo, uint32_t &hi) {
-    const uint32_t magic = 0x64006400u;
-    uint32_t r0 = (x & 0x000F000Fu) | magic;
-    uint32_t r1 = (x & 0x00F000F0u) | magic;
-    lo = h2u(__hmul2(__hsub2(*reinterpret_cast<__half2 *>(&r0), __floats2half2_rn(1032.f, 1032.f)),
-                     s2));
-    hi = h2u(__hmul2(__hfma2(*reinterpret_cast<__half2 *>(&r1), __floats2half2_rn(0.0625f, 0.0625f),
-                             __floats2half2_rn(-72.f, -72.f)),
-                     s2));
-}
-
-// s2 = (s, s); c2 = (-24 s, -24 s) when FUSED
-template <bool FUSED>
-__device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, __half2 c2, uint32_t (&o)[4]) {
-    if (FUSED) {
-        const uint32_t magic16 = 0x4C004C00u, mask = 0x03C003C0u;
-        uint32_t r0 = (w & mask) | magic16;
-        uint32_t r1 = (rotr(w, 4) & mask) | magic16;
-        o[0] = h2u(__hfma2(*reinterpret_cast<__half2 *>(&r0), s2, c2));
-        o[1] = h2u(__hfma2(*reinterpret_cast<__half2 *>(&r1), s2, c2));
-    } else {
-        exact_pairs(rotr(w, 6), s2, o[0], o[1]);
-    }
-    exact_pairs(rotr(w, 14), s2, o[2], o[3]);
-}
-
-// SiLU(gate) * up of one gate/up lane pair, as the fp16 pair hi + lo of
-// the lane's parity: hi = fp16(a) for even lanes, lo = fp16(a - hi) for odd
-// ones.  Both lanes compute a (no divergent branch); v is the lane's
-// accumulator value, the partner's comes over a shuffle.  __expf and
-// __fdividef (relative error ~1e-6) are far inside the layer tolerance.
-// Sets *overflow when a finite a is beyond fp16 range.
-__device__ __forceinline__ uint16_t silu_mul_half(float v, int lane, bool &overflow) {
-    const float other = __shfl_xor_sync(0xffffffffu, v, 1);
-    const float gte = (lane & 1) ? other : v;
-    const float up = (lane & 1) ? v : other;
-    const float act = __fdividef(gte * up, 1.0f + __expf(-gte));
-    const __half hi = __float2half_rn(act);
-    const __half lo = __float2half_rn(act - __half2float(hi));
-    overflow |= fabsf(act) > 65504.0f && fabsf(act) < INFINITY;
-    return __half_as_ushort((lane & 1) ? lo : hi);
 }
 
 template <int KIND, int NT, int STAGES, int DQG, int NPROD, int MMAW>
@@ -370,7 +253,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
         auto walk = [&](auto round_robin) {
             constexpr bool kRR = decltype(round_robin)::value;
             for (; c < my_chunks; c += NPROD) {
-                if (!warp_wait_bar(&sm->consumed[s], phase ^ 1, sm, a.ctrl, 1)) break;
+                if (!warp_wait_bar(&sm->consumed[s], phase ^ 1, &sm->abort, a.ctrl, 1)) break;
                 if (elect_one()) {
                     // two copies per chunk: the weight block (codes and
                     // scales, contiguous) and the chunk's token rows
@@ -451,13 +334,13 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             const int n_mma = kCat ? 2 * NT : max(16, (t.rows + 15) & ~15);
             const uint32_t idesc = idesc_f16_m128((uint32_t)n_mma);
             const int acc = seg & 1;
-            if (!warp_wait_bar(&sm->acc_empty[acc], ((seg >> 1) & 1) ^ 1, sm, a.ctrl, 2)) break;
+            if (!warp_wait_bar(&sm->acc_empty[acc], ((seg >> 1) & 1) ^ 1, &sm->abort, a.ctrl, 2)) break;
             tc_fence_after();
             const uint32_t d_tmem = tb + kAccBase + (acc * MMAW + mw) * kAccCols;
             const int c_end = c + (k1 - k0);
             bool first = true;
             for (int cc = c + ((mw - c % MMAW) + MMAW) % MMAW; cc < c_end; cc += MMAW) {
-                if (!warp_wait_bar(&sm->a_full[b], bph, sm, a.ctrl, 3)) {
+                if (!warp_wait_bar(&sm->a_full[b], bph, &sm->abort, a.ctrl, 3)) {
                     ok = false;
                     break;
                 }
@@ -522,13 +405,13 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
         int s = grp, b = grp;
         uint32_t ph = 0;
         for (int c = grp; c < my_chunks; c += kDqGroups) {
-            if (!warp_wait_bar(&sm->full[s], ph, sm, a.ctrl, 4)) break;
+            if (!warp_wait_bar(&sm->full[s], ph, &sm->abort, a.ctrl, 4)) break;
             // A buffer b was last read by the MMAs of chunk c - kAB, whose
             // stage is kAB stages back
             if (c >= kAB) {
                 const int sp = s >= kAB ? s - kAB : s - kAB + STAGES;
                 const uint32_t pp = s >= kAB ? ph : ph ^ 1;
-                if (!warp_wait_bar(&sm->consumed[sp], pp, sm, a.ctrl, 5)) break;
+                if (!warp_wait_bar(&sm->consumed[sp], pp, &sm->abort, a.ctrl, 5)) break;
             }
             tc_fence_after();
             const uint8_t *st = base + s * kStageBytes + kTokBoxes * kTokBox;
@@ -592,7 +475,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             const int k1 = k0 + (segment_end(c_seg, k0) - c_seg);
             const Tile t = decode_tile<NT>(a, sm, tile);
             const int acc = seg & 1;
-            if (!warp_wait_bar(&sm->acc_full[acc], (seg >> 1) & 1, sm, a.ctrl, 6)) break;
+            if (!warp_wait_bar(&sm->acc_full[acc], (seg >> 1) & 1, &sm->abort, a.ctrl, 6)) break;
             tc_fence_after();
             const uint32_t acc_addr = tb + lane_off + kAccBase + acc * MMAW * kAccCols;
             // with two issuers, the second one had a chunk here unless the

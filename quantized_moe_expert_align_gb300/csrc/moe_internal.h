@@ -81,6 +81,7 @@ AlignLayout align_layout(int M, int k, int E);
 
 // Carving of the forward workspace.
 struct FwdLayout {
+    bool fused;         // the whole layer in one kernel (small batches, decode.cu)
     int nt;             // token rows per MMA tile of the gate+up GEMM
     int nt2;            // token rows per MMA tile of the down GEMM (<= nt)
     int max_tok_tiles;  // bound on sum_e ceil(count_e / nt)
@@ -88,8 +89,9 @@ struct FwdLayout {
     int grid;           // most CTAs the GEMM kernels may use (partials are sized for it)
     size_t ctrl, counts, offsets, tile_prefix, tile_prefix2, perm, inv_perm;
     size_t seg_counts, seg_base;  // int32 [E][kAlignSegs] each, large batches only
-    size_t tickets;     // int32 [max_tok_tiles * 4 * 2I/128 + max_tok_tiles2 * 4 * H/128]
-    size_t partials;    // fp32 [grid][2][nt][128]
+    size_t tickets;     // int32 [max_tok_tiles * 4 * 2I/128 + max_tok_tiles2 * 4 * H/128];
+                        // fused: the single kernel's sync region (decode_sync_ints)
+    size_t partials;    // fp32 [grid][2][nt][128], fused: [2][grid][2][nt][128]
     size_t xs;          // [n][H] fp16 hidden rows in sorted order
     size_t act_hi;      // [n][I] fp16
     size_t act_lo;      // [n][I] fp16
@@ -100,6 +102,9 @@ struct FwdLayout {
 // gate+up GEMM, and for the down GEMM given the former.
 int pick_token_tile(int n, int E);
 int down_token_tile(int nt);
+// Whether a batch of n slots with gate+up token tiles of nt rows runs as the
+// single small-batch kernel.
+bool use_decode_kernel(int64_t n, int nt);
 FwdLayout fwd_layout(int M, int k, int E, int H, int I);
 
 // moe_w4a16_forward on a scratch buffer the caller of this function chose.
