@@ -51,7 +51,7 @@ namespace cg = cooperative_groups;
 constexpr int kNT = kDecodeTokenTile;                 // token rows per tile
 constexpr int kStages = 12;
 constexpr int kDqGroups = 4;
-constexpr int kWProd = 2;                             // weight producer warps
+constexpr int kWProd = 2;                             // producer warps (alternate chunks)
 constexpr int kMmaWarps = 2;
 constexpr int kEpiWarps = 4;
 constexpr int kAB = 4;                                // TMEM A buffers
@@ -64,8 +64,7 @@ constexpr int kAccBase = kAB * kACols;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kWarpDq = kEpiWarps;
 constexpr int kWarpWProd = kWarpDq + 4 * kDqGroups;
-constexpr int kWarpTProd = kWarpWProd + kWProd;
-constexpr int kWarpMma = kWarpTProd + 1;
+constexpr int kWarpMma = kWarpWProd + kWProd;
 constexpr int kWarps = kWarpMma + kMmaWarps;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxSlots = kDecodeMaxSlots;
@@ -233,33 +232,6 @@ __device__ __forceinline__ uint32_t half_bits(float v) {
     return (uint32_t)__half_as_ushort(__float2half_rn(v));
 }
 
-// Bounded wait until the flag reaches `target` (lane 0 polls; the warp gets
-// the verdict).
-__device__ __forceinline__ bool warp_wait_flag(const int32_t *flag, int target, Smem *sm, Ctrl *ctrl,
-                                               int lane) {
-    int ok = 1;
-    if (lane == 0) {
-        if (ld_acquire(flag) < target) {
-            const long long t0 = clock64();
-            for (;;) {
-                __nanosleep(256);
-                if (ld_acquire(flag) >= target) break;
-                if (*(volatile int *)&sm->abort) {
-                    ok = 0;
-                    break;
-                }
-                if (clock64() - t0 > kWaitCycles) {
-                    atomicExch(&sm->abort, 1);
-                    set_status(ctrl, MOE_ERR_DEVICE_TIMEOUT, 7);
-                    ok = 0;
-                    break;
-                }
-            }
-        }
-    }
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap map_x,
                   const __grid_constant__ CUtensorMap map_act) {
@@ -300,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm->first_bad_slot = kMaxSlots;
         fence_barrier_init();
     }
-    if (warp == kWarpTProd && lane == 0) {
+    if (warp == kWarpWProd && lane == 0) {
         prefetch_tensormap(&map_x);
         prefetch_tensormap(&map_act);
     }
@@ -466,36 +438,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // The weight producers issue their first copies now: the weights are
-    // the call's input and the stages are free.
-    Walker wk;
+    // ---------------- producers, set-up.  Producer pw copies the weight
+    // block and the token rows of chunks pw, pw + 2, ... (global order: the
+    // gate+up chunks, then the down chunks).  The weights are the call's
+    // input, so the copies into the first (free) stages go out now; token
+    // rows wait for the barrier below.
+    const bool producer = warp >= kWarpWProd && warp < kWarpMma;
+    const int pw = warp - kWarpWProd;
+    Walker wk, tk;       // the next chunk whose weights / token rows to copy
+    int wgc = pw, tgc = pw;
     bool w_more = false;
-    int w_gc = 0;
     const uint64_t pol_w = policy_evict_first();
-    auto issue_weights = [&]() {
-        const int s = w_gc % kStages;
-        const uint32_t par = ((w_gc / kStages) & 1) ^ 1;
-        if (!warp_wait_bar(&sm->consumed[s], par, &sm->abort, a.ctrl, 1)) return false;
+    auto issue_weights = [&](int s) {
         if (elect_one()) {
-            uint8_t *st = base + s * kStageBytes;
             mbar_arrive_expect_tx(&sm->wfull[s], kBlockBytes);
-            bulk_g2s_hint(st + kTokBytes, wk.blk + (int64_t)wk.kc * kBlockBytes, kBlockBytes,
-                          &sm->wfull[s], pol_w);
+            bulk_g2s_hint(base + s * kStageBytes + kTokBytes, wk.blk + (int64_t)wk.kc * kBlockBytes,
+                          kBlockBytes, &sm->wfull[s], pol_w);
         }
         __syncwarp();
-        return true;
+        wgc += kWProd;
+        w_more = wk.advance(kWProd, m[0], m[1], sm, g, G);
     };
-    if (warp >= kWarpWProd && warp < kWarpTProd) w_gc = warp - kWarpWProd;
-    if (warp >= kWarpWProd && warp < kWarpTProd && !a.test_no_copies) {
-        w_more = wk.start(w_gc, m[0], m[1], sm, g, G);
-        while (w_more && w_gc < kStages) {
-            if (!issue_weights()) {
-                w_more = false;
-                break;
-            }
-            w_gc += kWProd;
-            w_more = wk.advance(kWProd, m[0], m[1], sm, g, G);
-        }
+    if (producer && !a.test_no_copies) {
+        w_more = wk.start(pw, m[0], m[1], sm, g, G);
+        tk.start(pw, m[0], m[1], sm, g, G);
+        while (w_more && wgc < kStages) issue_weights(wgc);  // fresh stages: free
     }
 
     // grid-wide barrier: xs, the zeroed tickets and flags are complete.
@@ -525,55 +492,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     // are waited for
     const bool run = !*(volatile int *)&sm->abort;
 
-    if (warp >= kWarpWProd && warp < kWarpTProd) {
-        // ---------------- weight producers (alternate chunks)
-        const int pw = warp - kWarpWProd;
-        if (!*(volatile int *)&sm->abort) {
-            while (w_more) {  // (never true with the failure-path switch)
-                if (!issue_weights()) break;
-                w_gc += kWProd;
-                w_more = wk.advance(kWProd, m[0], m[1], sm, g, G);
+    if (producer) {
+        // ---------------- producers.  A chunk's token rows go out once its
+        // weights have (its stage is then free) and, for a down-GEMM chunk,
+        // once the gate+up tiles that write its activation rows are done;
+        // a chunk waiting for that flag does not hold back later chunks'
+        // weight copies, so the down GEMM's weights stream (and are
+        // dequantised) while the gate+up GEMM finishes elsewhere.
+        if (run) {
+            fence_proxy_async_global();
+            long long idle_since = clock64();
+            for (;;) {
+                bool progressed = false;
+                // token rows of chunks whose weights are on their way, in order
+                while (tgc < wgc) {
+                    const int s = tgc % kStages;
+                    if (tk.ph == 1) {
+                        int ready = 0;
+                        if (lane == 0)
+                            ready = ld_acquire(flags + (int64_t)tk.t.v * KC2 + tk.kc) >= kFlagTarget;
+                        if (!__shfl_sync(0xffffffffu, ready, 0)) break;
+                        fence_proxy_async_global();
+                    }
+                    if (elect_one()) {
+                        uint8_t *st = base + s * kStageBytes;
+                        if (tk.ph == 0) {
+                            mbar_arrive_expect_tx(&sm->tfull[s], 2 * kTokBox);
+                            tma_load_3d(st, &map_x, 0, tk.t.p0, 2 * tk.kc, &sm->tfull[s]);
+                        } else {
+                            mbar_arrive_expect_tx(&sm->tfull[s], 4 * kTokBox);
+                            tma_load_4d(st, &map_act, 0, tk.t.p0, 0, 2 * tk.kc, &sm->tfull[s]);
+                        }
+                    }
+                    __syncwarp();
+                    tgc += kWProd;
+                    tk.advance(kWProd, m[0], m[1], sm, g, G);
+                    progressed = true;
+                }
+                // the next weight block, if its stage is free
+                if (w_more) {
+                    const int s = wgc % kStages;
+                    const uint32_t par = ((wgc / kStages) & 1) ^ 1;
+                    int free_ = 0;
+                    if (lane == 0) free_ = mbar_test_wait(&sm->consumed[s], par);
+                    if (__shfl_sync(0xffffffffu, free_, 0)) {
+                        issue_weights(s);
+                        progressed = true;
+                    } else if (tgc == wgc) {
+                        // nothing but the stage to wait for: sleep on it
+                        if (!warp_wait_bar(&sm->consumed[s], par, &sm->abort, a.ctrl, 1)) break;
+                        issue_weights(s);
+                        progressed = true;
+                    }
+                }
+                if (!w_more && tgc >= wgc) break;
+                if (progressed) {
+                    idle_since = clock64();
+                    continue;
+                }
+                // waiting for a flag (and perhaps a stage): poll, bounded
+                if (*(volatile int *)&sm->abort) break;
+                if (clock64() - idle_since > kWaitCycles) {
+                    atomicExch(&sm->abort, 1);
+                    set_status(a.ctrl, MOE_ERR_DEVICE_TIMEOUT, 7);
+                    break;
+                }
+                __nanosleep(128);
             }
         }
         // every copy issued must land before the CTA exits
-        for (int j = (w_gc > kStages ? w_gc - kStages : 0); j < w_gc; ++j)
+        for (int j = (wgc > kStages ? wgc - kStages : 0); j < wgc; ++j)
             if (j % kWProd == pw) wait_bar_final(&sm->wfull[j % kStages], (j / kStages) & 1);
+        for (int j = (tgc > kStages ? tgc - kStages : 0); j < tgc; ++j)
+            if (j % kWProd == pw) wait_bar_final(&sm->tfull[j % kStages], (j / kStages) & 1);
         __syncwarp();
     } else if (!run) {
         // nothing to do
-    } else if (warp == kWarpTProd) {
-        // ---------------- token producer (every chunk): the sorted hidden
-        // rows for the gate+up GEMM, the activation rows for the down GEMM
-        // once the gate+up tiles that write them are done
-        fence_proxy_async_global();
-        Walker tw;
-        int gc = 0;
-        bool more = tw.start(0, m[0], m[1], sm, g, G);
-        while (more) {
-            const int s = gc % kStages;
-            if (!warp_wait_bar(&sm->consumed[s], ((gc / kStages) & 1) ^ 1, &sm->abort, a.ctrl, 1)) break;
-            if (tw.ph == 1) {
-                if (!warp_wait_flag(flags + (int64_t)tw.t.v * KC2 + tw.kc, kFlagTarget, sm, a.ctrl, lane))
-                    break;
-                fence_proxy_async_global();
-            }
-            if (elect_one()) {
-                uint8_t *st = base + s * kStageBytes;
-                if (tw.ph == 0) {
-                    mbar_arrive_expect_tx(&sm->tfull[s], 2 * kTokBox);
-                    tma_load_3d(st, &map_x, 0, tw.t.p0, 2 * tw.kc, &sm->tfull[s]);
-                } else {
-                    mbar_arrive_expect_tx(&sm->tfull[s], 4 * kTokBox);
-                    tma_load_4d(st, &map_act, 0, tw.t.p0, 0, 2 * tw.kc, &sm->tfull[s]);
-                }
-            }
-            __syncwarp();
-            ++gc;
-            more = tw.advance(1, m[0], m[1], sm, g, G);
-        }
-        for (int j = (gc > kStages ? gc - kStages : 0); j < gc; ++j)
-            wait_bar_final(&sm->tfull[j % kStages], (j / kStages) & 1);
-        __syncwarp();
     } else if (warp >= kWarpMma) {
         // ---------------- MMA issuers (alternate chunks, own accumulators)
         const int mw = warp - kWarpMma;

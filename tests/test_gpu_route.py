@@ -146,15 +146,25 @@ def _routed_forward(dl, wl, M, rows=None):
     return moe.moe_w4a16_get_diag()
 
 
+def _launches(M, k):
+    """Kernels of a forward from logits: the router then the single
+    small-batch kernel (at most 128 slots); above that the five kernels,
+    routing inside the alignment kernel up to 64 tokens, else a router
+    kernel first."""
+    if M * k <= 128:
+        return 2
+    return 5 if M <= 64 else 6
+
+
 def test_forward_routed_toy(toy_layer):
     d = _routed_forward(toy_layer, synth.TOY, 4)
-    assert d["kernels_launched"] == 5
+    assert d["kernels_launched"] == _launches(4, synth.TOY.layer.k)
 
 
 @pytest.mark.parametrize("M", [1, 9, 90])
 def test_forward_routed_decode(e384_layer, M):
     d = _routed_forward(e384_layer, synth.DECODE, M, rows=None if M < 90 else gu.sample_rows(M, 24))
-    assert d["kernels_launched"] == (5 if M <= 64 else 6)
+    assert d["kernels_launched"] == _launches(M, synth.DECODE.layer.k)
 
 
 def test_forward_routed_second_shape(e128_layer):
