@@ -12,7 +12,7 @@ each under ``other_workloads``.
   python bench.py [--gpus N] [--steps K] [--warmup W]
                   [--config decode|plateau|prefill|second|toy|e256|group128]
                   [--extra plateau,prefill,second|none]
-                  [--impl ours|reference]
+                  [--small-batch-kernel five|one] [--impl ours|reference]
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the plain CPU
 oracle on a bounded sample of the same workload instead.  Under torchrun
@@ -713,6 +713,7 @@ def our_arm(args, wl):
                        "k": L.k, "group": L.group,
                        "routing": "zipf(1.1)-biased" if wl.zipf_s else "uniform",
                        "l2": "flushed before every call (write of 2x L2, outside the events)",
+                       "small_batch_kernel": args.small_batch_kernel,
                        "parallelism": f"replicas x{world}",
                        "vs_baseline_ref": "pages' sweep on one RTX PRO 6000 (sm_120): context"},
             "clocks": clocks, "e2e": e2e, "gpu_launches": gpu_launches,
@@ -742,6 +743,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-slots", type=int, default=800,
                     help="slots the CPU-baseline oracle sample covers")
+    ap.add_argument("--small-batch-kernel", choices=["five", "one"], default="five",
+                    help="batches of at most 128 slots: the five kernels (default) or the "
+                         "opt-in single kernel (MOE_W4A16_DECODE_FUSED=1)")
     ap.add_argument("--extra", default=None,
                     help="comma-separated further workloads timed in the same run "
                          "(default with the decode sweep: plateau,prefill,second; "
@@ -756,6 +760,8 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     wl = CONFIGS[args.config]
+    if args.small_batch_kernel == "one":
+        os.environ["MOE_W4A16_DECODE_FUSED"] = "1"   # read by the library at its first call
     if args.impl == "reference":
         return reference_arm(args, wl)
     return our_arm(args, wl)

@@ -191,13 +191,14 @@ size_t moe_w4a16_workspace_size(int M, int k, int E, int H, int I);
  * Numerics: weights dequantised exactly to fp16, hidden converted to fp16
  * (values beyond fp16 range set MOE_ERR_DEVICE_FP16_RANGE), fp32
  * accumulation, the activation passed to the down GEMM as an fp16 hi+lo pair.
- * Kernels: batches of at most 128 slots (M*k) whose token tile is 16 rows
- * run as one cooperative kernel of one CTA per SM (every CTA resident at
- * once; the call fails with MOE_ERR_CUDA where the device cannot host
- * that); larger ones as five kernels (alignment, hidden gather, gate+up
- * GEMM, down GEMM, combine).  For testing, MOE_W4A16_DECODE_FUSED=0 (read
- * once per process) sends small batches through the five kernels too.
- * Either way the same results are written to `out` and to the workspace.
+ * Kernels: five (alignment, hidden gather, gate+up GEMM, down GEMM,
+ * combine), chained with programmatic dependent launch.  Opt-in:
+ * MOE_W4A16_DECODE_FUSED=1 (read once per process) runs batches of at most
+ * 128 slots (M*k) whose token tile is 16 rows as one cooperative kernel of
+ * one CTA per SM (every CTA resident at once; the call fails with
+ * MOE_ERR_CUDA where the device cannot host that) -- the same results,
+ * written to `out` and to the workspace; on one GB300 it measured 7-10%
+ * slower than the five kernels, hence off by default.
  */
 moe_status_t moe_w4a16_forward(const uint16_t *hidden, const int32_t *topk_ids,
                                const float *topk_w, const void *w13, const void *w2,

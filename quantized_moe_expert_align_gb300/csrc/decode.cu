@@ -94,8 +94,7 @@ struct Gemm {
 };
 
 struct Smem {
-    uint64_t wfull[kStages];     // weight block landed
-    uint64_t tfull[kStages];     // token rows landed
+    uint64_t full[kStages];      // weight block and token rows landed
     uint64_t consumed[kStages];  // MMAs of the stage's chunk done
     uint64_t a_full[kAB];
     uint64_t acc_full[2], acc_empty[2];
@@ -188,15 +187,23 @@ __device__ __forceinline__ Tile decode_tile(const Smem *sm, int R, int tile) {
 }
 
 // Walks a producer's chunks over both GEMMs (gate+up first), `step` chunks
-// at a time, looking the tile up only when a run of chunks in one tile ends.
-// It keeps its own copy of the current GEMM (a runtime index into a pair
-// would put the pair in local memory).
+// at a time: within a tile it only moves the weight pointer; a round-robin
+// walk steps to the tile G further on without a division; only the start,
+// the stream-K part and the change of GEMM use the full lookup.  It keeps
+// its own copy of the current GEMM (a runtime index into a pair would put
+// the pair in local memory).
 struct Walker {
     Gemm cur;
-    int ph, c, kc, end;
-    const uint8_t *blk;  // K chunk 0 of the current tile's weight blocks
-    Tile t;
+    int ph, c, kc, end, tile;
+    const uint8_t *wp;  // the weight block of the current chunk
+    int p0, v;          // the current tile's first sorted row and token tile
 
+    __device__ __forceinline__ void at_tile(const Smem *sm) {
+        const Tile t = decode_tile(sm, cur.R, tile);
+        p0 = t.p0;
+        v = t.v;
+        wp = cur.w + kHeaderBytes + (((int64_t)t.e * cur.R + t.rt) * cur.KC + kc) * kBlockBytes;
+    }
     __device__ __forceinline__ bool settle(const Gemm &m0, const Gemm &m1, const Smem *sm, int g,
                                            int G) {
         if (ph == 0 && c >= m0.my) {
@@ -205,11 +212,9 @@ struct Walker {
             cur = m1;
         }
         if (c >= cur.my) return false;
-        int tile;
         locate(cur, g, G, c, tile, kc);
         end = seg_end(cur, c, kc);
-        t = decode_tile(sm, cur.R, tile);
-        blk = cur.w + kHeaderBytes + ((int64_t)t.e * cur.R + t.rt) * cur.KC * kBlockBytes;
+        at_tile(sm);
         return true;
     }
     __device__ __forceinline__ bool start(int gc, const Gemm &m0, const Gemm &m1, const Smem *sm,
@@ -222,8 +227,21 @@ struct Walker {
     __device__ __forceinline__ bool advance(int step, const Gemm &m0, const Gemm &m1, const Smem *sm,
                                             int g, int G) {
         c += step;
-        kc += step;
-        if (c < end) return true;
+        if (c < end) {
+            kc += step;
+            wp += (int64_t)step * kBlockBytes;
+            return true;
+        }
+        if (cur.rr && c < cur.my) {
+            kc += step;
+            do {
+                kc -= cur.KC;
+                tile += G;
+            } while (kc >= cur.KC);
+            end = c - kc + cur.KC;
+            at_tile(sm);
+            return true;
+        }
         return settle(m0, m1, sm, g, G);
     }
 };
@@ -253,8 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&sm->wfull[s], 1);
-            mbar_init(&sm->tfull[s], 1);
+            mbar_init(&sm->full[s], 1);
             mbar_init(&sm->consumed[s], 1);
         }
         for (int b = 0; b < kAB; ++b) mbar_init(&sm->a_full[b], 128);
@@ -276,6 +293,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&map_x);
         prefetch_tensormap(&map_act);
     }
+
+    // The hidden rows are the call's input: this thread's first 16-byte
+    // piece of them goes out now, before the alignment says where it goes.
+    const int64_t gthreads = (int64_t)G * kThreads, gi = (int64_t)g * kThreads + tid;
+    const int vecs = a.H / 8;
+    const int64_t hwork = (int64_t)a.M * vecs;
+    uint4 hv0 = make_uint4(0, 0, 0, 0);
+    if (gi < hwork)
+        hv0 = __ldg(reinterpret_cast<const uint4 *>(a.hidden + (size_t)(gi / vecs) * a.H) + gi % vecs);
 
     // ---------------- alignment of the <= 128 slots, in shared memory: the
     // stable counting sort by expert of the flat index f = t*k + j
@@ -365,10 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_tt = sm->bad ? 0 : n_tt_all;  // a mismatched buffer: no GEMM work
     // the two GEMMs' schedules live in shared memory: every role reads the
     // fields it needs instead of holding both in registers
-    if (tid == 0) {
-        make_gemm(sm->gm[0], a.w13, R1, KC1, n_tt, G, g);
-        make_gemm(sm->gm[1], a.w2, R2, KC2, n_tt, G, g);
-    }
+    if (tid == 0) make_gemm(sm->gm[0], a.w13, R1, KC1, n_tt, G, g);
+    if (tid == 32) make_gemm(sm->gm[1], a.w2, R2, KC2, n_tt, G, g);
     __syncthreads();
     const Gemm *m = sm->gm;
     const int total = m[0].my + m[1].my;  // this CTA's chunks over both GEMMs
@@ -380,20 +404,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t *flags = tick2 + (int64_t)m[1].T * kEpiWarps;
     int32_t *comb = flags + (int64_t)n_tt * KC2;
     const int64_t sync_used = (int64_t)(comb - a.sync) + (int64_t)R2 * kEpiWarps;
-    const int64_t gthreads = (int64_t)G * kThreads, gi = (int64_t)g * kThreads + tid;
 
     // ---------------- prologue across the grid
     if (sync_used <= a.sync_ints)
         for (int64_t i = gi; i < sync_used; i += gthreads) a.sync[i] = 0;
     {
-        // hidden rows -> fp16, in sorted order
-        const int vecs = a.H / 8;
-        const int64_t work = (int64_t)n_valid * vecs;
+        // hidden rows -> fp16, each piece written to the sorted rows of its
+        // token's valid slots
         bool overflow = false;
-        for (int64_t i = gi; i < work; i += gthreads) {
-            const int p = (int)(i / vecs), v = (int)(i % vecs);
-            const int t = sm->perm[p] / a.k;
-            const uint4 in = __ldg(reinterpret_cast<const uint4 *>(a.hidden + (size_t)t * a.H) + v);
+        for (int64_t i = gi; i < hwork; i += gthreads) {
+            const int t = (int)(i / vecs), v = (int)(i % vecs);
+            const uint4 in = (i == gi) ? hv0
+                                       : __ldg(reinterpret_cast<const uint4 *>(a.hidden + (size_t)t * a.H) + v);
             const uint32_t w[4] = {in.x, in.y, in.z, in.w};
             uint32_t o[4];
 #pragma unroll
@@ -403,7 +425,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 overflow |= (fabsf(lo) > 65504.0f && !isinf(lo)) || (fabsf(hi) > 65504.0f && !isinf(hi));
                 o[j] = half_bits(lo) | (half_bits(hi) << 16);
             }
-            reinterpret_cast<uint4 *>(a.xs + (size_t)p * a.H)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+            const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+            for (int j = 0; j < a.k; ++j) {
+                const int p = sm->inv[t * a.k + j];
+                if (p >= 0) reinterpret_cast<uint4 *>(a.xs + (size_t)p * a.H)[v] = ov;
+            }
         }
         if (overflow) sm->overflow = 1;
         // no token tile at all (every id out of range): the output is zero
@@ -413,56 +439,86 @@ __global__ void __launch_bounds__(kThreads, 1)
                 reinterpret_cast<uint4 *>(a.out)[i] = make_uint4(0, 0, 0, 0);
         }
     }
-    if (g == 0) {
-        // the alignment, for inspection (the views of the workspace)
-        for (int e = tid; e < a.E; e += kThreads) {
-            int lo = 0, hi = n_act;  // first active index with act_e >= e
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (sm->act_e[mid] < e) lo = mid + 1; else hi = mid;
-            }
-            a.offsets[e] = sm->act_off[lo];
-            a.counts[e] = (lo < n_act && sm->act_e[lo] == e) ? sm->act_off[lo + 1] - sm->act_off[lo] : 0;
+    if (g == 0 && tid == 0) {
+        if (a.reset_status) {
+            a.ctrl->status = 0;
+            a.ctrl->detail = 0;
         }
-        if (tid == 0) a.offsets[a.E] = n_valid;
-        for (int p = tid; p < n; p += kThreads) {
-            a.perm[p] = p < n_valid ? sm->perm[p] : -1;
-            a.inv_perm[p] = sm->inv[p];
-        }
-        if (tid == 0) {
-            if (a.reset_status) {
-                a.ctrl->status = 0;
-                a.ctrl->detail = 0;
-            }
-            a.ctrl->n_invalid = n - n_valid;
-        }
+        a.ctrl->n_invalid = n - n_valid;
     }
 
     // ---------------- producers, set-up.  Producer pw copies the weight
     // block and the token rows of chunks pw, pw + 2, ... (global order: the
-    // gate+up chunks, then the down chunks).  The weights are the call's
-    // input, so the copies into the first (free) stages go out now; token
-    // rows wait for the barrier below.
+    // gate+up chunks, then the down chunks) into the chunk's stage, both
+    // counted on the stage's `full` barrier.  The weights are the call's
+    // input, so the copies into the first (free) stages go out now; their
+    // token rows follow the grid barrier below.
     const bool producer = warp >= kWarpWProd && warp < kWarpMma;
     const int pw = warp - kWarpWProd;
-    Walker wk, tk;       // the next chunk whose weights / token rows to copy
-    int wgc = pw, tgc = pw;
-    bool w_more = false;
+    Walker wk;           // the next chunk whose copies are not issued
+    int wgc = pw;        // its global index
+    bool more = false;
     const uint64_t pol_w = policy_evict_first();
     auto issue_weights = [&](int s) {
         if (elect_one()) {
-            mbar_arrive_expect_tx(&sm->wfull[s], kBlockBytes);
-            bulk_g2s_hint(base + s * kStageBytes + kTokBytes, wk.blk + (int64_t)wk.kc * kBlockBytes,
-                          kBlockBytes, &sm->wfull[s], pol_w);
+            mbar_arrive_expect_tx(&sm->full[s], kBlockBytes + (wk.ph ? 4 : 2) * kTokBox);
+            bulk_g2s_hint(base + s * kStageBytes + kTokBytes, wk.wp, kBlockBytes, &sm->full[s], pol_w);
         }
         __syncwarp();
-        wgc += kWProd;
-        w_more = wk.advance(kWProd, m[0], m[1], sm, g, G);
+    };
+    auto issue_tokens = [&](const Walker &w, int s) {
+        if (elect_one()) {
+            uint8_t *st = base + s * kStageBytes;
+            if (w.ph == 0)
+                tma_load_3d(st, &map_x, 0, w.p0, 2 * w.kc, &sm->full[s]);
+            else
+                tma_load_4d(st, &map_act, 0, w.p0, 0, 2 * w.kc, &sm->full[s]);
+        }
+        __syncwarp();
+    };
+    // Down-GEMM chunks need the gate+up tiles that write their activation
+    // rows to be done.  The producer reads the flags of 32 K chunks of one
+    // token tile with one warp-wide load (lane i: chunk base + i) and keeps
+    // which of them were complete (flags only grow), so a flag costs an L2
+    // round trip only when the producer reaches a chunk whose flag it has
+    // not yet seen complete.  Waits are bounded.
+    int ready_v = -1, ready_base = 0;
+    unsigned ready_mask = 0;  // bit i: flag (ready_v, ready_base + i) seen complete
+    auto wait_flag = [&](const Walker &w) {
+        const int base32 = w.kc & ~31, bit = w.kc - base32;
+        if (w.v == ready_v && base32 == ready_base && ((ready_mask >> bit) & 1u)) return true;
+        const long long t0 = clock64();
+        for (;;) {
+            const int kc = base32 + lane;
+            const bool ok = kc < KC2 && ld_acquire(flags + (int64_t)w.v * KC2 + kc) >= kFlagTarget;
+            ready_v = w.v;
+            ready_base = base32;
+            ready_mask = __ballot_sync(0xffffffffu, ok);
+            if ((ready_mask >> bit) & 1u) {
+                // the lane that issues the copy follows every lane's acquire
+                __syncwarp();
+                fence_proxy_async_global();
+                return true;
+            }
+            if (*(volatile int *)&sm->abort) return false;
+            if (clock64() - t0 > kWaitCycles) {
+                if (lane == 0) {
+                    atomicExch(&sm->abort, 1);
+                    set_status(a.ctrl, MOE_ERR_DEVICE_TIMEOUT, 7);
+                }
+                __syncwarp();
+                return false;
+            }
+            __nanosleep(256);
+        }
     };
     if (producer && !a.test_no_copies) {
-        w_more = wk.start(pw, m[0], m[1], sm, g, G);
-        tk.start(pw, m[0], m[1], sm, g, G);
-        while (w_more && wgc < kStages) issue_weights(wgc);  // fresh stages: free
+        more = wk.start(pw, m[0], m[1], sm, g, G);
+        while (more && wgc < kStages) {  // fresh stages: free
+            issue_weights(wgc);
+            wgc += kWProd;
+            more = wk.advance(kWProd, m[0], m[1], sm, g, G);
+        }
     }
 
     // grid-wide barrier: xs, the zeroed tickets and flags are complete.
@@ -493,78 +549,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool run = !*(volatile int *)&sm->abort;
 
     if (producer) {
-        // ---------------- producers.  A chunk's token rows go out once its
-        // weights have (its stage is then free) and, for a down-GEMM chunk,
-        // once the gate+up tiles that write its activation rows are done;
-        // a chunk waiting for that flag does not hold back later chunks'
-        // weight copies, so the down GEMM's weights stream (and are
-        // dequantised) while the gate+up GEMM finishes elsewhere.
-        if (run) {
+        // ---------------- producers.  First the token rows of the chunks
+        // whose weights went out before the barrier (each stage's
+        // transaction count includes them, so they are issued even after a
+        // failure), then one chunk at a time: wait for its stage, copy its
+        // weights, and copy its token rows -- for a down-GEMM chunk once the
+        // gate+up tiles that write them are done.
+        if (!a.test_no_copies) {
             fence_proxy_async_global();
-            long long idle_since = clock64();
-            for (;;) {
-                bool progressed = false;
-                // token rows of chunks whose weights are on their way, in order
-                while (tgc < wgc) {
-                    const int s = tgc % kStages;
-                    if (tk.ph == 1) {
-                        int ready = 0;
-                        if (lane == 0)
-                            ready = ld_acquire(flags + (int64_t)tk.t.v * KC2 + tk.kc) >= kFlagTarget;
-                        if (!__shfl_sync(0xffffffffu, ready, 0)) break;
-                        fence_proxy_async_global();
-                    }
+            bool ok = run;
+            if (pw < wgc) {
+                Walker tk;
+                tk.start(pw, m[0], m[1], sm, g, G);
+                for (int tgc = pw; tgc < wgc; tgc += kWProd) {
+                    if (tk.ph == 1 && ok) ok = wait_flag(tk);
+                    issue_tokens(tk, tgc % kStages);
+                    tk.advance(kWProd, m[0], m[1], sm, g, G);
+                }
+            }
+            // stage and its phase parity kept incrementally (no division per chunk)
+            int s = wgc % kStages;
+            uint32_t par = ((wgc / kStages) & 1) ^ 1;
+            while (ok && more) {
+                if (!warp_wait_bar(&sm->consumed[s], par, &sm->abort, a.ctrl, 1)) break;
+                const bool known = wk.ph == 0 || (wk.v == ready_v && (wk.kc & ~31) == ready_base &&
+                                                  ((ready_mask >> (wk.kc & 31)) & 1u));
+                if (known) {
+                    // the common case: both copies from one elected lane
                     if (elect_one()) {
                         uint8_t *st = base + s * kStageBytes;
-                        if (tk.ph == 0) {
-                            mbar_arrive_expect_tx(&sm->tfull[s], 2 * kTokBox);
-                            tma_load_3d(st, &map_x, 0, tk.t.p0, 2 * tk.kc, &sm->tfull[s]);
-                        } else {
-                            mbar_arrive_expect_tx(&sm->tfull[s], 4 * kTokBox);
-                            tma_load_4d(st, &map_act, 0, tk.t.p0, 0, 2 * tk.kc, &sm->tfull[s]);
-                        }
+                        mbar_arrive_expect_tx(&sm->full[s], kBlockBytes + (wk.ph ? 4 : 2) * kTokBox);
+                        bulk_g2s_hint(st + kTokBytes, wk.wp, kBlockBytes, &sm->full[s], pol_w);
+                        if (wk.ph == 0)
+                            tma_load_3d(st, &map_x, 0, wk.p0, 2 * wk.kc, &sm->full[s]);
+                        else
+                            tma_load_4d(st, &map_act, 0, wk.p0, 0, 2 * wk.kc, &sm->full[s]);
                     }
                     __syncwarp();
-                    tgc += kWProd;
-                    tk.advance(kWProd, m[0], m[1], sm, g, G);
-                    progressed = true;
+                } else {
+                    // the weights go out first; the activation rows once ready
+                    issue_weights(s);
+                    ok = wait_flag(wk);
+                    issue_tokens(wk, s);
                 }
-                // the next weight block, if its stage is free
-                if (w_more) {
-                    const int s = wgc % kStages;
-                    const uint32_t par = ((wgc / kStages) & 1) ^ 1;
-                    int free_ = 0;
-                    if (lane == 0) free_ = mbar_test_wait(&sm->consumed[s], par);
-                    if (__shfl_sync(0xffffffffu, free_, 0)) {
-                        issue_weights(s);
-                        progressed = true;
-                    } else if (tgc == wgc) {
-                        // nothing but the stage to wait for: sleep on it
-                        if (!warp_wait_bar(&sm->consumed[s], par, &sm->abort, a.ctrl, 1)) break;
-                        issue_weights(s);
-                        progressed = true;
-                    }
+                wgc += kWProd;
+                s += kWProd;
+                if (s >= kStages) {
+                    s -= kStages;
+                    par ^= 1;
                 }
-                if (!w_more && tgc >= wgc) break;
-                if (progressed) {
-                    idle_since = clock64();
-                    continue;
-                }
-                // waiting for a flag (and perhaps a stage): poll, bounded
-                if (*(volatile int *)&sm->abort) break;
-                if (clock64() - idle_since > kWaitCycles) {
-                    atomicExch(&sm->abort, 1);
-                    set_status(a.ctrl, MOE_ERR_DEVICE_TIMEOUT, 7);
-                    break;
-                }
-                __nanosleep(128);
+                more = wk.advance(kWProd, m[0], m[1], sm, g, G);
             }
         }
         // every copy issued must land before the CTA exits
         for (int j = (wgc > kStages ? wgc - kStages : 0); j < wgc; ++j)
-            if (j % kWProd == pw) wait_bar_final(&sm->wfull[j % kStages], (j / kStages) & 1);
-        for (int j = (tgc > kStages ? tgc - kStages : 0); j < tgc; ++j)
-            if (j % kWProd == pw) wait_bar_final(&sm->tfull[j % kStages], (j / kStages) & 1);
+            if (j % kWProd == pw) wait_bar_final(&sm->full[j % kStages], (j / kStages) & 1);
         __syncwarp();
     } else if (!run) {
         // nothing to do
@@ -574,6 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t desc_base = sdesc_k_sw128(smem_u32(base));
         int seg = 0;
         bool ok = true;
+        // stage, A buffer and A-buffer phase of this warp's next chunk, kept
+        // incrementally (kStages and kAB are multiples of kMmaWarps)
+        int s = mw, b = mw;
+        uint32_t bph = 0;
 #pragma unroll
         for (int ph = 0; ph < 2; ++ph) {
             if (!ok) break;
@@ -595,9 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int gc = gbase + c;
                 gc += ((mw - gc % kMmaWarps) + kMmaWarps) % kMmaWarps;
                 for (; gc < gbase + c_end; gc += kMmaWarps) {
-                    const int s = gc % kStages, b = gc % kAB;
-                    if (!warp_wait_bar(&sm->tfull[s], (gc / kStages) & 1, &sm->abort, a.ctrl, 3) ||
-                        !warp_wait_bar(&sm->a_full[b], (gc / kAB) & 1, &sm->abort, a.ctrl, 3)) {
+                    // the dequant warps arrive on a_full after their wait on the
+                    // stage's full barrier, which also counted the token rows
+                    if (!warp_wait_bar(&sm->a_full[b], bph, &sm->abort, a.ctrl, 3)) {
                         ok = false;
                         break;
                     }
@@ -616,6 +659,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     __syncwarp();
                     first = false;
+                    s += kMmaWarps;
+                    if (s >= kStages) s -= kStages;
+                    b += kMmaWarps;
+                    if (b >= kAB) {
+                        b -= kAB;
+                        bph ^= 1;
+                    }
                 }
                 if (!ok) break;
                 if (elect_one()) tc_commit(&sm->acc_full[acc]);
@@ -633,14 +683,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int grp = (warp - kWarpDq) / 4;
         const int r = (warp & 3) * 32 + lane;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const int my0 = m[0].my;
+        const bool wide0 = sm->wide[0] != 0, wide1 = sm->wide[1] != 0;
+        // stage, its phase and the A buffer of this group's next chunk, kept
+        // incrementally (kStages and kAB are multiples of kDqGroups)
+        int s = grp, b = grp;
+        uint32_t ph = 0;
         for (int gc = grp; gc < total; gc += kDqGroups) {
-            const int s = gc % kStages, b = gc % kAB;
-            if (!warp_wait_bar(&sm->wfull[s], (gc / kStages) & 1, &sm->abort, a.ctrl, 4)) break;
+            if (!warp_wait_bar(&sm->full[s], ph, &sm->abort, a.ctrl, 4)) break;
             if (gc >= kAB) {
-                const int gp = gc - kAB;  // A buffer b was last read by chunk gp's MMAs
-                if (!warp_wait_bar(&sm->consumed[gp % kStages], (gp / kStages) & 1, &sm->abort,
-                                   a.ctrl, 5))
-                    break;
+                // A buffer b was last read by the MMAs of chunk gc - kAB,
+                // whose stage is kAB stages back
+                const int sp = s >= kAB ? s - kAB : s - kAB + kStages;
+                const uint32_t pp = s >= kAB ? ph : ph ^ 1;
+                if (!warp_wait_bar(&sm->consumed[sp], pp, &sm->abort, a.ctrl, 5)) break;
             }
             tc_fence_after();
             const uint32_t st_s = smem_u32(base + s * kStageBytes + kTokBytes);
@@ -673,16 +729,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st16(a_addr + pc * 16, v);
                 }
             };
-            if (sm->wide[gc < m[0].my ? 0 : 1])
+            if (gc < my0 ? wide0 : wide1)
                 pieces(std::false_type{});
             else
                 pieces(std::true_type{});
             tc_wait_st();
             tc_fence_before();
             mbar_arrive(&sm->a_full[b]);
+            s += kDqGroups;
+            if (s >= kStages) {
+                s -= kStages;
+                ph ^= 1;
+            }
+            b += kDqGroups;
+            if (b >= kAB) b -= kAB;
         }
     } else {
         // ---------------- epilogue warpgroup (warps 0-3)
+        if (g == 0) {
+            // the alignment, for inspection (the views of the workspace),
+            // written while the first tiles are still being computed
+            for (int e = tid; e < a.E; e += (32 * kEpiWarps)) {
+                int lo = 0, hi = n_act;  // first active index with act_e >= e
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (sm->act_e[mid] < e) lo = mid + 1; else hi = mid;
+                }
+                a.offsets[e] = sm->act_off[lo];
+                a.counts[e] = (lo < n_act && sm->act_e[lo] == e) ? sm->act_off[lo + 1] - sm->act_off[lo] : 0;
+            }
+            if (tid == 0) a.offsets[a.E] = n_valid;
+            for (int p = tid; p < n; p += (32 * kEpiWarps)) {
+                a.perm[p] = p < n_valid ? sm->perm[p] : -1;
+                a.inv_perm[p] = sm->inv[p];
+            }
+        }
         const int r = warp * 32 + lane;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         int seg = 0;
@@ -800,18 +881,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (lane == 0) last = (atomicAdd(comb + t.rt * kEpiWarps + warp, 1) == n_tt - 1);
                         if (__shfl_sync(0xffffffffu, last, 0)) {
                             // every token's k slots for output column h, in
-                            // ascending slot order, one bf16 rounding
+                            // ascending slot order (the flat slot order),
+                            // one bf16 rounding; the y loads of 8 slots go
+                            // out together
                             __threadfence();
                             const int h = t.rt * kTileRows + r;
-                            for (int tok = 0; tok < a.M; ++tok) {
-                                float sum = 0.f;
-                                for (int j = 0; j < a.k; ++j) {
-                                    const int pos = sm->inv[tok * a.k + j];
-                                    if (pos < 0) continue;
-                                    const float wv = __ldg(a.topk_w + (size_t)tok * a.k + j);
-                                    sum = fmaf(wv, __ldcg(a.y + (size_t)pos * a.H + h), sum);
+                            float sum = 0.f;
+                            for (int f0 = 0; f0 < n; f0 += 8) {
+                                float yv[8], wv[8];
+                                int pv[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const int f = f0 + i;
+                                    pv[i] = f < n ? sm->inv[f] : -1;
+                                    wv[i] = pv[i] >= 0 ? __ldg(a.topk_w + f) : 0.f;
+                                    yv[i] = pv[i] >= 0 ? __ldcg(a.y + (size_t)pv[i] * a.H + h) : 0.f;
                                 }
-                                a.out[(size_t)tok * a.H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const int f = f0 + i;
+                                    if (f >= n) break;
+                                    if (pv[i] >= 0) sum = fmaf(wv[i], yv[i], sum);
+                                    if ((f + 1) % a.k == 0) {
+                                        a.out[(size_t)(f / a.k) * a.H + h] =
+                                            __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+                                        sum = 0.f;
+                                    }
+                                }
                             }
                         }
                     }

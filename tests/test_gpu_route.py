@@ -147,12 +147,8 @@ def _routed_forward(dl, wl, M, rows=None):
 
 
 def _launches(M, k):
-    """Kernels of a forward from logits: the router then the single
-    small-batch kernel (at most 128 slots); above that the five kernels,
-    routing inside the alignment kernel up to 64 tokens, else a router
-    kernel first."""
-    if M * k <= 128:
-        return 2
+    """Kernels of a forward from logits: the five kernels, the alignment
+    kernel routing first up to 64 tokens, else a router kernel first."""
     return 5 if M <= 64 else 6
 
 
