@@ -45,7 +45,9 @@ CONFIGS = {"decode": synth.DECODE, "plateau": synth.PLATEAU, "prefill": synth.PR
 # The pages' sweep on one RTX PRO 6000 (sm_120), context only: ms per call.
 PAGES_MS = {1: 0.151, 9: 1.18, 90: 5.19, 256: 7.02, 512: 7.01, 1024: 7.02}
 KERNELS = ["align", "gather", "gemm_gate_up", "gemm_down", "combine"]
-FUSED_KERNEL = "decode_fused"   # small batches: the whole layer in one kernel
+# small batches (at most 128 slots): one kernel aligns and gathers
+SMALL_KERNELS = ["align_gather", None, "gemm_gate_up", "gemm_down", "combine"]
+FUSED_KERNEL = "decode_fused"   # opt-in: the whole layer in one kernel
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum, one ncu pass,
 # caches flushed by ncu before each launch) of the gate+up GEMM launches of
@@ -289,8 +291,8 @@ def layer_rows(wl, batches, call_ms, kernel_ms, hbm_peak, tf_peak):
         t_hbm = roof_bytes / (hbm_peak * 1e9)
         t_tc = flops / (tf_peak * 1e12)
         t_roof_ms = 1e3 * max(t_hbm, t_tc)
-        k_ms, fused = kernel_ms[M]
-        names = [FUSED_KERNEL] if fused else KERNELS
+        k_ms, mode = kernel_ms[M]
+        names = {"one": [FUSED_KERNEL], "small": SMALL_KERNELS}.get(mode, KERNELS)
         rows.append({
             "M": M, "active_experts": active,
             "us_per_call": round(1e3 * call_ms[M], 2),
@@ -299,7 +301,7 @@ def layer_rows(wl, batches, call_ms, kernel_ms, hbm_peak, tf_peak):
             "roofline_bytes": roof_bytes, "roofline_flops": flops,
             "roofline_us": round(1e3 * t_roof_ms, 2),
             "frac_of_roofline": round(t_roof_ms / call_ms[M], 4),
-            "kernel_ms": {n: round(float(v), 5) for n, v in zip(names, k_ms)},
+            "kernel_ms": {n: round(float(v), 5) for n, v in zip(names, k_ms) if n},
             "us_per_call_profiled": round(1e3 * float(k_ms.sum()), 2),
             "pages_ms_rtx_pro_6000": PAGES_MS.get(M) if L.E == 384 else None,
         })
@@ -378,8 +380,9 @@ class Bench:
         return {M: [a.elapsed_time(b) for a, b in ev[M]] for M in Ms}
 
     def kernel_times(self, wl, devb, ws, reps):
-        """Per M: (mean ms of each library kernel, whether the call ran as the
-        single small-batch kernel) -- events between kernels
+        """Per M: (mean ms of each library kernel, the path: "five" kernels,
+        "small" -- four, one aligning and gathering -- or "one" for the opt-in
+        single kernel) -- events between kernels
         (moe_w4a16_forward_profiled), L2 flushed before every call.  The
         single kernel's time is the first entry."""
         torch, moe, L = self.torch, self.moe, wl.layer
@@ -395,10 +398,11 @@ class Bench:
                                                     L.I, ws.buf, evs, self.stream)
                 if st != moe.MOE_OK:
                     raise moe.MoeError(st, "moe_w4a16_forward_profiled")
-                fused[M] = moe.moe_w4a16_get_diag()["kernels_launched"] == 1
+                fused[M] = {1: "one", 4: "small"}.get(moe.moe_w4a16_get_diag()["kernels_launched"],
+                                                     "five")
                 torch.cuda.synchronize()
                 per[M] += np.array([evs[i].elapsed_time(evs[i + 1]) for i in range(5)])
-        return {M: (per[M][:1] if fused[M] else per[M]) / reps for M in wl.Ms}, fused
+        return {M: (per[M][:1] if fused[M] == "one" else per[M]) / reps for M in wl.Ms}, fused
 
     def check_status(self, ws, what):
         moe = self.moe

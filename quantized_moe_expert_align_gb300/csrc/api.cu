@@ -9,6 +9,7 @@
 #include "gemm_tc.h"
 #include "moe_internal.h"
 #include "route.cuh"
+#include "small_align.cuh"
 
 namespace moe {
 
@@ -125,6 +126,7 @@ FwdLayout fwd_layout(int M, int k, int E, int H, int I) {
                         : take(((size_t)l.max_tok_tiles * (2 * I / kTileRows) +
                                 (size_t)l.max_tok_tiles2 * (H / kTileRows)) * 4 * 4);
     l.partials = take((size_t)(l.fused ? 2 : 1) * l.grid * 2 * l.nt * kTileRows * 4);
+    l.ovf = take((size_t)kMaxGrid * 4);
     l.xs = take(n * H * 2);
     l.act_hi = take(n * I * 2);
     l.act_lo = take(n * I * 2);
@@ -532,6 +534,37 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
         return MOE_OK;
     }
     const bool pdl = (ev == nullptr);
+    if (!logits && n <= kSmallAlignSlots) {
+        // Small batch: one kernel aligns (in every CTA) and gathers, then the
+        // two GEMMs and the combine.
+        const int pg = small_prep_grid(M, H);
+        SmallPrepArgs sp = {ids, hidden, M, k, E, H, L.nt, L.nt2, counts, offsets, tile_prefix,
+                            tile_prefix2, perm, inv_perm, xs, ctrl, clear,
+                            reinterpret_cast<int32_t *>(ws + L.ovf)};
+        g1.ovf = sp.ovf;
+        g1.n_ovf = pg;
+        g1.tables_after_wait = 1;
+        if (mark(0) != cudaSuccess || launch_align_gather_small(sp, pg, s) != cudaSuccess ||
+            mark(1) != cudaSuccess || mark(2) != cudaSuccess ||
+            launch_gemm_tc(g1, map_x, grid, s, pdl) != cudaSuccess || mark(3) != cudaSuccess ||
+            launch_gemm_tc(g2, map_act, grid, s, pdl) != cudaSuccess || mark(4) != cudaSuccess ||
+            launch_combine(cb, s, pdl) != cudaSuccess || mark(5) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+        g_diag.M = M;
+        g_diag.k = k;
+        g_diag.E = E;
+        g_diag.H = H;
+        g_diag.I = I;
+        g_diag.token_tile = L.nt;
+        g_diag.grid_gemm1 = grid;
+        g_diag.grid_gemm2 = grid;
+        g_diag.kernels_launched = 4;
+        g_diag.workspace_bytes = (int64_t)L.total;
+        g_diag.calls += 1;
+        return MOE_OK;
+    }
     bool route_kernel = false;
     set_segments(al, ws, L.seg_counts, L.seg_base);
     if (begin_call(al, logits, M, k, const_cast<int32_t *>(ids), const_cast<float *>(topk_w), s,

@@ -39,6 +39,7 @@
 #include "decode.h"
 #include "device_common.cuh"
 #include "sm100.cuh"
+#include "small_align.cuh"
 #include "tc_common.cuh"
 
 namespace moe {
@@ -68,6 +69,7 @@ constexpr int kWarpMma = kWarpWProd + kWProd;
 constexpr int kWarps = kWarpMma + kMmaWarps;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxSlots = kDecodeMaxSlots;
+static_assert(kMaxSlots == kSmallAlignSlots, "the alignment of a small batch");
 // a down-GEMM chunk (128 activation columns) is ready once both gate+up
 // tiles that write them have had all four epilogue warps count it
 constexpr int kFlagTarget = 2 * kEpiWarps;
@@ -104,17 +106,10 @@ struct Smem {
     int bad;                     // a prepacked header does not match
     int wide[2];                 // per matrix: scales beyond the fused dequantisation
     int overflow;                // a hidden value beyond fp16 range
-    int first_bad_slot;
-    int warp_starts[4];
-    int n_valid, n_act, n_tt;
+    int n_tt;
     Gemm gm[2];                  // this CTA's view of the gate+up and the down GEMM
-    int32_t raw[kMaxSlots];      // the slot's id as given
-    int32_t sid[kMaxSlots];      // the slot's id, or -1 outside [0, E)
-    int32_t perm[kMaxSlots];     // sorted row -> slot
-    int32_t inv[kMaxSlots];      // slot -> sorted row, or -1
-    int32_t act_e[kMaxSlots + 1];    // active experts, ascending
-    int32_t act_off[kMaxSlots + 1];  // their first sorted row (act_off[n_act] = n_valid)
-    int32_t act_tp[kMaxSlots + 1];   // their first token tile (act_tp[n_act] = n_tt)
+    SmallAlign al;               // the batch's alignment
+    int32_t act_tp[kMaxSlots + 1];   // active experts' first token tile (act_tp[n_act] = n_tt)
 };
 
 __device__ __forceinline__ int ld_acquire(const int32_t *p) {
@@ -175,14 +170,14 @@ __device__ __forceinline__ Tile decode_tile(const Smem *sm, int R, int tile) {
     Tile t;
     t.v = tile / R;
     t.rt = tile - t.v * R;
-    int lo = 0, hi = sm->n_act;  // largest a with act_tp[a] <= v
+    int lo = 0, hi = sm->al.n_act;  // largest a with act_tp[a] <= v
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
         if (sm->act_tp[mid] <= t.v) lo = mid; else hi = mid;
     }
-    t.e = sm->act_e[lo];
-    t.p0 = sm->act_off[lo] + (t.v - sm->act_tp[lo]) * kNT;
-    t.rows = min(kNT, sm->act_off[lo + 1] - t.p0);
+    t.e = sm->al.act_e[lo];
+    t.p0 = sm->al.act_off[lo] + (t.v - sm->act_tp[lo]) * kNT;
+    t.rows = min(kNT, sm->al.act_off[lo + 1] - t.p0);
     return t;
 }
 
@@ -286,7 +281,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm->wide[0] = reinterpret_cast<const PackHeader *>(a.w13)->wide_scales != 0;
         sm->wide[1] = reinterpret_cast<const PackHeader *>(a.w2)->wide_scales != 0;
         sm->overflow = 0;
-        sm->first_bad_slot = kMaxSlots;
         fence_barrier_init();
     }
     if (warp == kWarpWProd && lane == 0) {
@@ -303,85 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (gi < hwork)
         hv0 = __ldg(reinterpret_cast<const uint4 *>(a.hidden + (size_t)(gi / vecs) * a.H) + gi % vecs);
 
-    // ---------------- alignment of the <= 128 slots, in shared memory: the
-    // stable counting sort by expert of the flat index f = t*k + j
-    int id = -1;
-    if (tid < n) {
-        const int raw = __ldg(a.ids + tid);
-        id = (raw >= 0 && raw < a.E) ? raw : -1;
-        sm->raw[tid] = raw;
-        sm->sid[tid] = id;
-    }
-    const int n_valid = __syncthreads_count(tid < n && id >= 0);
-    if (tid < n) {
-        if (id >= 0) {
-            int pos = 0;
-            for (int f = 0; f < n; ++f) {
-                const int o = sm->sid[f];
-                pos += (o >= 0) & ((o < id) | ((o == id) & (f < tid)));
-            }
-            sm->inv[tid] = pos;
-            sm->perm[pos] = tid;
-        } else {
-            sm->inv[tid] = -1;
-            atomicMin(&sm->first_bad_slot, tid);
-        }
-    }
-    __syncthreads();
-    // active experts: the sorted rows where the expert changes, ranked by a
-    // ballot over the first four warps
-    bool start = false;
-    int e_here = -1;
-    if (tid < n_valid) {
-        e_here = sm->sid[sm->perm[tid]];
-        start = (tid == 0) || (sm->sid[sm->perm[tid - 1]] != e_here);
-    }
-    unsigned ballot = 0;
-    if (warp < 4) {
-        ballot = __ballot_sync(0xffffffffu, start);
-        if (lane == 0) sm->warp_starts[warp] = __popc(ballot);
-    }
-    __syncthreads();
-    if (warp < 4) {
-        int rank = __popc(ballot & ((1u << lane) - 1u));
-        for (int w = 0; w < warp; ++w) rank += sm->warp_starts[w];
-        if (start) {
-            sm->act_e[rank] = e_here;
-            sm->act_off[rank] = tid;
-        }
-    }
-    const int n_act = sm->warp_starts[0] + sm->warp_starts[1] + sm->warp_starts[2] + sm->warp_starts[3];
-    if (tid == 0) sm->act_off[n_act] = n_valid;
-    __syncthreads();
-    // token tiles per active expert, exclusive prefix (one warp, four
-    // experts per lane)
+    // ---------------- alignment of the <= 128 slots, in shared memory
+    small_align(&sm->al, a.ids, n, a.E);
+    const int n_valid = sm->al.n_valid, n_act = sm->al.n_act;
     if (warp == 0) {
-        int cnt[4], sum = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int ai = lane * 4 + i;
-            cnt[i] = ai < n_act ? (sm->act_off[ai + 1] - sm->act_off[ai] + kNT - 1) / kNT : 0;
-            sum += cnt[i];
-        }
-        int incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        int run = incl - sum;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int ai = lane * 4 + i;
-            if (ai < n_act) sm->act_tp[ai] = run;
-            run += cnt[i];
-        }
-        if (lane == 31) {
-            sm->act_tp[n_act] = incl;
-            sm->n_tt = incl;
-            sm->n_valid = n_valid;
-            sm->n_act = n_act;
-        }
+        const int tt = small_tile_prefix(&sm->al, kNT, sm->act_tp, lane);
+        if (lane == 0) sm->n_tt = tt;
     }
     tc_fence_before();
     __syncthreads();
@@ -427,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
             for (int j = 0; j < a.k; ++j) {
-                const int p = sm->inv[t * a.k + j];
+                const int p = sm->al.inv[t * a.k + j];
                 if (p >= 0) reinterpret_cast<uint4 *>(a.xs + (size_t)p * a.H)[v] = ov;
             }
         }
@@ -535,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (tid == 0) {
         if (g == 0 && sm->bad) set_status(a.ctrl, MOE_ERR_BAD_LAYOUT, 0);
-        if (g == 0 && n_valid < n) set_status(a.ctrl, MOE_ERR_DEVICE_BAD_EXPERT_ID, sm->raw[sm->first_bad_slot]);
+        if (g == 0 && n_valid < n) set_status(a.ctrl, MOE_ERR_DEVICE_BAD_EXPERT_ID, sm->al.raw[sm->al.first_bad_slot]);
         if (sm->overflow) set_status(a.ctrl, MOE_ERR_DEVICE_FP16_RANGE, 0);
         if (sync_used > a.sync_ints) {
             set_status(a.ctrl, MOE_ERR_DEVICE_TIMEOUT, 0);  // cannot happen: sized on the host
@@ -750,18 +671,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the alignment, for inspection (the views of the workspace),
             // written while the first tiles are still being computed
             for (int e = tid; e < a.E; e += (32 * kEpiWarps)) {
-                int lo = 0, hi = n_act;  // first active index with act_e >= e
-                while (lo < hi) {
-                    const int mid = (lo + hi) >> 1;
-                    if (sm->act_e[mid] < e) lo = mid + 1; else hi = mid;
-                }
-                a.offsets[e] = sm->act_off[lo];
-                a.counts[e] = (lo < n_act && sm->act_e[lo] == e) ? sm->act_off[lo + 1] - sm->act_off[lo] : 0;
+                const int lo = small_first_at_least(&sm->al, e);
+                a.offsets[e] = sm->al.act_off[lo];
+                a.counts[e] = (lo < n_act && sm->al.act_e[lo] == e)
+                                  ? sm->al.act_off[lo + 1] - sm->al.act_off[lo] : 0;
             }
             if (tid == 0) a.offsets[a.E] = n_valid;
             for (int p = tid; p < n; p += (32 * kEpiWarps)) {
-                a.perm[p] = p < n_valid ? sm->perm[p] : -1;
-                a.inv_perm[p] = sm->inv[p];
+                a.perm[p] = p < n_valid ? sm->al.perm[p] : -1;
+                a.inv_perm[p] = sm->al.inv[p];
             }
         }
         const int r = warp * 32 + lane;
@@ -893,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                                 for (int i = 0; i < 8; ++i) {
                                     const int f = f0 + i;
-                                    pv[i] = f < n ? sm->inv[f] : -1;
+                                    pv[i] = f < n ? sm->al.inv[f] : -1;
                                     wv[i] = pv[i] >= 0 ? __ldg(a.topk_w + f) : 0.f;
                                     yv[i] = pv[i] >= 0 ? __ldcg(a.y + (size_t)pv[i] * a.H + h) : 0.f;
                                 }

@@ -169,11 +169,23 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
         if (sm->bad && g == 0) set_status(a.ctrl, MOE_ERR_BAD_LAYOUT, KIND);
         fence_barrier_init();
     }
+    if (warp == kProducerWarp && lane == 0) prefetch_tensormap(&tok);
+    // The tile tables come from an earlier kernel of the call.  When that is
+    // the kernel right before this one, wait for it to complete first.
+    // Either way this kernel lets the next one start only after reading
+    // them, and that one reads the same tables in its own set-up: every
+    // kernel's early start follows the completion of all kernels before its
+    // predecessor.
+    if (a.tables_after_wait) pdl_wait();
     for (int i = tid; i <= a.E; i += kThreads) {
         sm->tile_prefix[i] = __ldg(a.tile_prefix + i);
         sm->offsets[i] = __ldg(a.offsets + i);
     }
-    if (warp == kProducerWarp && lane == 0) prefetch_tensormap(&tok);
+    if (a.n_ovf > 0 && g == 0 && warp == 0) {
+        int any = 0;
+        for (int i = lane; i < a.n_ovf; i += 32) any |= a.ovf[i];
+        if (__any_sync(0xffffffffu, any) && lane == 0) set_status(a.ctrl, MOE_ERR_DEVICE_FP16_RANGE, 0);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -559,7 +571,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             if (!whole) {
                 // Fixed-order reduction by whichever CTA finishes the tile
                 // last; each warp handles its own 32 rows with its own ticket.
-                // The previous kernel of the call (the hidden-row gather)
+                // An earlier kernel of the call (the hidden-row gather)
                 // zeroes the tickets: this atomic must stay ordered after the
                 // producers' griddepcontrol.wait, which it is through the
                 // full -> MMA -> acc_full chain that led here.

@@ -21,6 +21,15 @@ struct TcArgs {
     uint16_t *act_hi, *act_lo;   // gate+up output [n][I] fp16
     float *y;                    // down output [n][H] fp32
     Ctrl *ctrl;
+    // Per-CTA fp16-overflow flags of the small-batch alignment-and-gather
+    // kernel (n_ovf of them, null otherwise); the gate+up GEMM reports any.
+    const int32_t *ovf;
+    int n_ovf;
+    // Nonzero: the kernel right before this one wrote the tile tables (the
+    // small-batch kernel before the gate+up GEMM), so the set-up waits for it
+    // before reading them; otherwise the tables are older and the set-up
+    // reads them at once, overlapping the previous kernel.
+    int tables_after_wait;
     // Failure-path test switch: nonzero makes the producers issue no copies,
     // so the other roles' bounded waits run out (MOE_ERR_DEVICE_TIMEOUT) and
     // the CTA winds down; zero in normal use.

@@ -92,6 +92,7 @@ struct FwdLayout {
     size_t tickets;     // int32 [max_tok_tiles * 4 * 2I/128 + max_tok_tiles2 * 4 * H/128];
                         // fused: the single kernel's sync region (decode_sync_ints)
     size_t partials;    // fp32 [grid][2][nt][128], fused: [2][grid][2][nt][128]
+    size_t ovf;         // int32 [grid]: per-CTA fp16-overflow flags of the small-batch kernel
     size_t xs;          // [n][H] fp16 hidden rows in sorted order
     size_t act_hi;      // [n][I] fp16
     size_t act_lo;      // [n][I] fp16

@@ -144,3 +144,12 @@ def test_prefill_zipf_e384(e384_layer, M, heavy_full):
     rows = gu.sample_rows(M, 16)
     gu.parity(gu.bf16_dev_to_f64(out)[rows], e384_layer.oracle(x, ids, w, rows),
               f"{wl.name} M={M} sampled tokens")
+
+
+def test_small_batch_path(e128_layer):
+    """Batches of at most 128 slots run four kernels (one aligns in every
+    CTA and gathers), larger ones five; both match the oracle in full."""
+    import quantized_moe_expert_align_gb300 as moe
+    for M, kernels in ((16, 4), (17, 5)):
+        _full(e128_layer, synth.SECOND, M)
+        assert moe.moe_w4a16_get_diag()["kernels_launched"] == kernels
