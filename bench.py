@@ -57,10 +57,10 @@ FUSED_KERNEL = "decode_fused"   # opt-in: the whole layer in one kernel
 # longer describes the kernel and the bench reports traffic as null.
 TRAFFIC_CAPTURE = {
     "kernel": "gemm_gate_up",
-    "sources_sha256": "901e484ff0c5ecfa6fed37872673523693baa9d8ed0bb1e84fc9822c2e079ec4",
+    "sources_sha256": "4aec2d514b722c4cd87d252e5022b1d521d3f951ed3bd0049401b9b509250fdd",
     "workload": "decode_e384_h7168_i2048_top8",
-    "bytes_per_launch": {1: 132315904 + 2819072, 9: 1091143424 + 558592,
-                         90: 5559521792 + 1895680},
+    "bytes_per_launch": {1: 132317184 + 2791936, 9: 1091124480 + 554240,
+                         90: 5559577344 + 2222336},
     "profile": "profiles/dram_gemm_gate_up_decode_e384_m1_9_90.md",
 }
 KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "tc_common.cuh", "sm100.cuh", "moe_internal.h",
