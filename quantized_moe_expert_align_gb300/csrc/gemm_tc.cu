@@ -243,11 +243,18 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
         // tile, K chunk, stage and stage phase incrementally: under the
         // dequantisation warps' load every instruction of this loop is slow
         // to issue, so it carries no per-chunk division or tile search.
-        // Each weight block is read once: it goes through L2 as evict-first,
-        // so that the token rows, which every 128-row weight tile of their
-        // expert reads again, stay in L2 (without the hint, at M = 1024 on
-        // E = 384 the gate+up GEMM read 1.86x its weight bytes from DRAM).
-        const uint64_t pol_w = policy_evict_first();
+        // An expert whose rows fit one token tile has its weights read once:
+        // they go through L2 as evict-first, so that the token rows, which
+        // every 128-row weight tile of their expert reads again, stay in L2
+        // (without the hint, at M = 1024 on E = 384 the gate+up GEMM read
+        // 1.86x its weight bytes from DRAM).  An expert with several token
+        // tiles has its weights streamed again for each of them, by CTAs
+        // working on its neighbouring tiles: those weights are kept in L2
+        // (evict-last) for the next token tile (Zipf prefill M = 16384
+        // 14.09 -> 13.35 ms, E = 128 M = 2048 979 -> 954 us in an A/B on one
+        // GPU; decode and plateau batches unchanged).
+        const uint64_t pol_first = policy_evict_first(), pol_keep = policy_evict_last();
+        uint64_t pol_w = pol_first;
         int c = pw, kc = 0, s = pw, p0 = 0, tile = 0;
         uint32_t phase = 0;
         int64_t blk0 = 0;
@@ -255,6 +262,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             const Tile t = decode_tile<NT>(a, sm, tile);
             blk0 = ((int64_t)t.e * R + t.rt) * KC;
             p0 = t.p0;
+            pol_w = (sm->tile_prefix[t.e + 1] - sm->tile_prefix[t.e] > 1) ? pol_keep : pol_first;
         };
         if (c < my_chunks) {
             locate_chunk(c, tile, kc);

@@ -91,6 +91,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
+// L2 eviction policy for data that will be read again soon.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
 // Contiguous global -> shared copy with an L2 eviction policy; dst, src
 // 16-byte aligned, bytes % 16 == 0; completes `bytes` on the mbarrier.
 __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes,
