@@ -57,10 +57,10 @@ FUSED_KERNEL = "decode_fused"   # opt-in: the whole layer in one kernel
 # longer describes the kernel and the bench reports traffic as null.
 TRAFFIC_CAPTURE = {
     "kernel": "gemm_gate_up",
-    "sources_sha256": "4aec2d514b722c4cd87d252e5022b1d521d3f951ed3bd0049401b9b509250fdd",
+    "sources_sha256": "238f10eda9f2b2fd8387b618e8edfe3c5874b7f091e3dc6337f5aca375aaf543",
     "workload": "decode_e384_h7168_i2048_top8",
-    "bytes_per_launch": {1: 132317184 + 2791936, 9: 1091124480 + 554240,
-                         90: 5559577344 + 2222336},
+    "bytes_per_launch": {1: 132318464 + 2811648, 9: 1091240704 + 519168,
+                         90: 5559526400 + 2526976},
     "profile": "profiles/dram_gemm_gate_up_decode_e384_m1_9_90.md",
 }
 KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "tc_common.cuh", "sm100.cuh", "moe_internal.h",
