@@ -465,8 +465,11 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
     CombineArgs cb = {y, inv_perm, topk_w, M, k, H, out};
 
     CUtensorMap map_x, map_act;
-    if (!make_token_map(&map_x, xs, n, H, L.nt) ||
-        !make_act_map(&map_act, act_hi, act_lo, n, I, L.nt2, stacked_hi_lo(L.nt2)))
+    // CTA pairs load half of the token rows (gate+up) or one of hi / lo (down)
+    const bool pair1 = tc_pair_mode(MOE_PACK_W13, L.nt, 2 * I);
+    const bool pair2 = tc_pair_mode(MOE_PACK_W2, L.nt2, H);
+    if (!make_token_map(&map_x, xs, n, H, pair1 ? L.nt / 2 : L.nt) ||
+        !make_act_map(&map_act, act_hi, act_lo, n, I, L.nt2, stacked_hi_lo(L.nt2), pair2))
         return MOE_ERR_CUDA;
 
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };

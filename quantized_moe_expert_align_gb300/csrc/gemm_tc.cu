@@ -37,6 +37,14 @@
 //    (stacked into one B operand for small token tiles).
 //  * An epilogue warpgroup drains the (double-buffered) accumulators while
 //    the next tile is being computed.
+//  * Large token tiles (128 rows in the gate+up GEMM, 64 in the down GEMM)
+//    run on CTA pairs (clusters of two, tcgen05 cta_group::2): a work tile
+//    is two neighbouring weight tiles, one per CTA, and one M = 256 MMA
+//    covers both, so each SM loads only half of the token operand.  One SM
+//    alone could not take in its 32 KiB of token rows per chunk as fast as
+//    its tensor core used them (E = 128 M = 2048: one chunk every ~740
+//    cycles against 512 of MMA work; as pairs the layer takes 898 instead of
+//    973 us, Zipf prefill M = 16384 11.2 instead of 13.8 ms).
 // Every mbarrier wait is bounded; a wait that gives up records
 // MOE_ERR_DEVICE_TIMEOUT and the CTA winds down without hanging.
 #include <cstring>
@@ -84,10 +92,16 @@ struct Tile {
     int e, rt, p0, rows;
 };
 
-template <int NT>
+// MMA N of a gate+up tile of `rows` token rows on a CTA pair: a multiple of
+// 32, so that each CTA's half of the token rows is a multiple of 16.
+__device__ __forceinline__ int pair_n(int rows) { return max(32, (rows + 31) & ~31); }
+
+// Work tile -> expert, first 128-row weight tile, token tile.  With CTA
+// pairs (CG = 2) a work tile is two neighbouring weight tiles, one per CTA.
+template <int NT, int CG>
 __device__ __forceinline__ Tile decode_tile(const TcArgs &a, const Smem *sm, int tile) {
     Tile t;
-    const int R = a.N / kTileRows;
+    const int R = a.N / kTileRows / CG;
     const int v = tile / R;
     int lo = 0, hi = a.E;  // largest e with tile_prefix[e] <= v (tile_prefix[E] > v)
     while (hi - lo > 1) {
@@ -100,22 +114,30 @@ __device__ __forceinline__ Tile decode_tile(const TcArgs &a, const Smem *sm, int
     // tile before moving to the next token tile
     const int local = tile - R * tp0;
     (void)tp1;
-    t.rt = local % R;
+    t.rt = (local % R) * CG;
     const int tt = local / R;
     t.p0 = sm->offsets[lo] + tt * NT;
     t.rows = min(NT, sm->offsets[lo + 1] - t.p0);
     return t;
 }
 
-template <int KIND, int NT, int STAGES, int DQG, int NPROD, int MMAW>
+// CG = 2: the kernel runs on clusters of two CTAs (CTA pairs, on the two SMs
+// of a TPC) that share each MMA (cta_group::2, M = 256): the even CTA issues
+// the pair's MMAs, each CTA dequantises its own 128-row weight tile into its
+// own tensor memory and holds its own 128 rows of the accumulators, and each
+// loads half of the token operand (the N side of the MMA): the first / second
+// half of the token rows (gate+up) or the hi / lo rows (down).
+template <int KIND, int NT, int STAGES, int DQG, int NPROD, int MMAW, int CG>
 __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     gemm_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tok) {
     constexpr int kDqGroups = DQG;
     constexpr int kThreads = threads_for(DQG, NPROD, MMAW);
     constexpr int kProducerWarp = kEpiWarps + 4 * DQG;
     constexpr int kMmaWarp = kProducerWarp + NPROD;
-    constexpr int kTokBox = NT * 128;                        // one 64-column box
-    constexpr int kTokBoxes = (KIND == MOE_PACK_W2) ? 4 : 2;  // hi(+lo) x 2 boxes
+    constexpr bool kPair = CG == 2;
+    constexpr int kTokRows = (kPair && KIND == MOE_PACK_W13) ? NT / 2 : NT;  // rows per box here
+    constexpr int kTokBox = kTokRows * 128;                   // one 64-column box
+    constexpr int kTokBoxes = (KIND == MOE_PACK_W2 && !kPair) ? 4 : 2;  // hi(+lo) x 2 boxes
     constexpr int kStageBytes = kTokBoxes * kTokBox + kBlockBytes;
     // Down GEMM with small token tiles: the hi and lo rows of a are stacked
     // into one B operand of 2*NT rows, so one MMA (whose cost does not grow
@@ -137,6 +159,11 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     // (a down-GEMM build with 5 A buffers and 2 issuers ran into exactly
     // that: its bounded waits gave up and reported MOE_ERR_DEVICE_TIMEOUT).
     static_assert(kAB % MMAW == 0 && STAGES % MMAW == 0, "each A buffer must belong to one MMA warp");
+    static_assert(!kPair || (MMAW == 1 && (KIND == MOE_PACK_W13 || kCat)),
+                  "CTA pairs: one MMA issuer; the down GEMM's hi and lo rows split between the CTAs");
+    // mbarrier arrivals: every dequant / epilogue thread of this CTA, or, on
+    // CTA pairs, one per warp of both CTAs (on the even CTA's barriers)
+    constexpr uint32_t kArrive = kPair ? 8u : 128u;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
@@ -146,21 +173,29 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, g = blockIdx.x;
     const int R = a.N / kTileRows, KC = a.K / kChunkK;
+    // CTA pairs: rank in the pair (0 issues the MMAs), pair index, pairs
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    const int gs = kPair ? g >> 1 : g, GS = kPair ? G >> 1 : G;
 
     // ---------------- setup
     if (warp == kMmaWarp) {
-        tmem_alloc(&sm->tmem_base, kTmemCols);
-        tmem_relinquish();
+        if (kPair) {
+            tmem_alloc_pair(&sm->tmem_base, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&sm->tmem_base, kTmemCols);
+            tmem_relinquish();
+        }
     }
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&sm->full[s], 1);
             mbar_init(&sm->consumed[s], 1);
         }
-        for (int b = 0; b < kAB; ++b) mbar_init(&sm->a_full[b], 128);
+        for (int b = 0; b < kAB; ++b) mbar_init(&sm->a_full[b], kArrive);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm->acc_full[b], MMAW);
-            mbar_init(&sm->acc_empty[b], 128);
+            mbar_init(&sm->acc_empty[b], kArrive);
         }
         mbar_init(&sm->done, MMAW);
         sm->abort = 0;
@@ -188,6 +223,8 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     }
     tc_fence_before();
     __syncthreads();
+    // the other CTA of a pair arrives on this one's barriers from now on
+    if (kPair) cluster_sync();
     tc_fence_after();
     pdl_trigger();
 
@@ -201,18 +238,20 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     // takes q whole tiles rem + g, rem + g + G, ...  Every CTA thus ends on
     // a whole tile, whose epilogue needs no fix-up: the ticketed reductions
     // of split tiles happen while the other CTAs are still streaming.
-    const int T = sm->bad ? 0 : sm->tile_prefix[a.E] * R;
-    const bool rr = T >= 8 * G;
+    // (CTA pairs: work tiles of two weight tiles, always whole tiles
+    // round-robin over the pairs)
+    const int T = sm->bad ? 0 : sm->tile_prefix[a.E] * (R / CG);
+    const bool rr = kPair || T >= 8 * G;
     const int q_whole = rr ? 0 : T / G;
     const int rem = rr ? 0 : T - q_whole * G;
     const int64_t W = (int64_t)rem * KC;  // stream-K units (tile * KC + chunk)
     const int64_t u_begin = range_begin(g, W, G), u_end = range_begin(g + 1, W, G);
     const int sk_chunks = (int)(u_end - u_begin);  // this CTA's stream-K chunks
-    const int my_chunks = rr ? (g < T ? (T - g + G - 1) / G : 0) * KC : sk_chunks + q_whole * KC;
+    const int my_chunks = rr ? (gs < T ? (T - gs + GS - 1) / GS : 0) * KC : sk_chunks + q_whole * KC;
     // tile and K chunk of this CTA's chunk number c
     auto locate_chunk = [&](int c, int &tile, int &kc) {
         if (rr) {
-            tile = g + (c / KC) * G;
+            tile = gs + (c / KC) * GS;
             kc = c % KC;
         } else if (c < sk_chunks) {
             tile = (int)((u_begin + c) / KC);
@@ -259,9 +298,11 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
         uint32_t phase = 0;
         int64_t blk0 = 0;
         auto locate = [&]() {
-            const Tile t = decode_tile<NT>(a, sm, tile);
-            blk0 = ((int64_t)t.e * R + t.rt) * KC;
-            p0 = t.p0;
+            const Tile t = decode_tile<NT, CG>(a, sm, tile);
+            // (a CTA pair: this CTA's weight tile of the two and, gate+up,
+            // its half of the token rows)
+            blk0 = ((int64_t)t.e * R + t.rt + (int)rank) * KC;
+            p0 = t.p0 + ((kPair && KIND == MOE_PACK_W13) ? (int)rank * (pair_n(t.rows) / 2) : 0);
             pol_w = (sm->tile_prefix[t.e + 1] - sm->tile_prefix[t.e] > 1) ? pol_keep : pol_first;
         };
         if (c < my_chunks) {
@@ -284,6 +325,8 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                                   &sm->full[s], pol_w);
                     if (KIND == MOE_PACK_W13)
                         tma_load_3d(st, &tok, 0, p0, 2 * kc, &sm->full[s]);
+                    else if (kPair)  // this CTA's hi (rank 0) or lo rows, K 0-63 then 64-127
+                        tma_load_4d(st, &tok, 0, p0, (int)rank, 2 * kc, &sm->full[s]);
                     else if (kCat)  // [hi | lo] for K 0-63, then for K 64-127
                         tma_load_4d(st, &tok, 0, p0, 0, 2 * kc, &sm->full[s]);
                     else            // [hi K0-63 | hi K64-127 | lo K0-63 | lo K64-127]
@@ -302,7 +345,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                     if (kc >= KC) {
                         do {
                             kc -= KC;
-                            tile += G;
+                            tile += GS;
                         } while (kc >= KC);
                         if (c + NPROD < my_chunks) locate();
                     }
@@ -346,15 +389,17 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
         const uint64_t desc_base = sdesc_k_sw128(smem_u32(base));
         int c = 0, seg = 0;  // c: CTA-local index of the segment's first chunk
         bool ok = true;
-        while (c < my_chunks && ok) {
+        // (the odd CTA of a pair issues nothing: the even one's MMAs cover both)
+        while (c < my_chunks && ok && rank == 0) {
             int tile, k0;
             locate_chunk(c, tile, k0);
             const int k1 = k0 + (segment_end(c, k0) - c);
-            const Tile t = decode_tile<NT>(a, sm, tile);
-            const int n_mma = kCat ? 2 * NT : max(16, (t.rows + 15) & ~15);
-            const uint32_t idesc = idesc_f16_m128((uint32_t)n_mma);
+            const Tile t = decode_tile<NT, CG>(a, sm, tile);
+            const int n_mma = kCat ? 2 * NT : (kPair ? pair_n(t.rows) : max(16, (t.rows + 15) & ~15));
+            const uint32_t idesc = idesc_f16(kTileRows * CG, (uint32_t)n_mma);
             const int acc = seg & 1;
-            if (!warp_wait_bar(&sm->acc_empty[acc], ((seg >> 1) & 1) ^ 1, &sm->abort, a.ctrl, 2)) break;
+            if (!warp_wait_bar(&sm->acc_empty[acc], ((seg >> 1) & 1) ^ 1, &sm->abort, a.ctrl, 2))
+                break;
             tc_fence_after();
             const uint32_t d_tmem = tb + kAccBase + (acc * MMAW + mw) * kAccCols;
             const int c_end = c + (k1 - k0);
@@ -375,7 +420,11 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
 #pragma unroll
                     for (int j = 0; j < kChunkK / 16; ++j) {
                         const uint32_t acc_flag = (!first || j > 0) ? 1u : 0u;
-                        if (kCat) {
+                        if (kPair) {  // each CTA's stage: its token rows, K 0-63 then 64-127
+                            const uint32_t boff = (j >> 2) * kTokBox + (j & 3) * 32;
+                            mma_f16_ts_pair(d_tmem, a_tmem + j * 8, desc0 + (boff >> 4), idesc,
+                                            acc_flag);
+                        } else if (kCat) {
                             const uint32_t boff = (j >> 2) * 2 * kTokBox + (j & 3) * 32;
                             mma_f16_ts(d_tmem, a_tmem + j * 8, desc0 + (boff >> 4), idesc,
                                        acc_flag);
@@ -388,7 +437,10 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                                            desc0 + ((2 * kTokBox + boff) >> 4), idesc, 1u);
                         }
                     }
-                    tc_commit(&sm->consumed[s]);
+                    if (kPair)
+                        tc_commit_pair(&sm->consumed[s]);
+                    else
+                        tc_commit(&sm->consumed[s]);
                 }
                 __syncwarp();
                 first = false;
@@ -403,14 +455,23 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             if (!ok) break;
             // an issuer with no chunk in this segment still arrives (its
             // accumulator is then not read)
-            if (elect_one()) tc_commit(&sm->acc_full[acc]);
+            if (elect_one()) {
+                if (kPair)
+                    tc_commit_pair(&sm->acc_full[acc]);
+                else
+                    tc_commit(&sm->acc_full[acc]);
+            }
             __syncwarp();
             c = c_end;
             ++seg;
         }
-        // Every MMA issued has completed once `done` fires.
+        // Every MMA issued has completed once `done` fires (on CTA pairs the
+        // even CTA's commit arrives in both).
         if (elect_one()) {
-            tc_commit(&sm->done);
+            if (!kPair)
+                tc_commit(&sm->done);
+            else if (rank == 0)
+                tc_commit_pair(&sm->done);
             wait_bar_final(&sm->done, 0);
         }
         __syncwarp();
@@ -474,7 +535,18 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                 pieces(std::true_type{});
             tc_wait_st();
             tc_fence_before();
-            mbar_arrive(&sm->a_full[b]);
+            if (kPair) {
+                // one arrival per warp, on the even CTA's barrier
+                __syncwarp();
+                if (lane == 0) {
+                    if (rank == 0)
+                        mbar_arrive(&sm->a_full[b]);
+                    else
+                        mbar_arrive_remote(&sm->a_full[b], 0);
+                }
+            } else {
+                mbar_arrive(&sm->a_full[b]);
+            }
             s += kDqGroups;
             if (s >= STAGES) {
                 s -= STAGES;
@@ -493,9 +565,10 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             int tile, k0;
             locate_chunk(c_seg, tile, k0);
             const int k1 = k0 + (segment_end(c_seg, k0) - c_seg);
-            const Tile t = decode_tile<NT>(a, sm, tile);
+            const Tile t = decode_tile<NT, CG>(a, sm, tile);
             const int acc = seg & 1;
             if (!warp_wait_bar(&sm->acc_full[acc], (seg >> 1) & 1, &sm->abort, a.ctrl, 6)) break;
+            const int rt = t.rt + (int)rank;  // this CTA's weight tile
             tc_fence_after();
             const uint32_t acc_addr = tb + lane_off + kAccBase + acc * MMAW * kAccCols;
             // with two issuers, the second one had a chunk here unless the
@@ -544,7 +617,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                             // even lanes write hi, odd lanes lo, of act
                             // column rt*64 + r/2
                             uint16_t *dst = ((lane & 1) ? a.act_lo : a.act_hi) +
-                                            (size_t)(t.p0 + c0) * a.I + t.rt * (kTileRows / 2) +
+                                            (size_t)(t.p0 + c0) * a.I + rt * (kTileRows / 2) +
                                             (r >> 1);
                             bool overflow = false;
 #pragma unroll
@@ -558,7 +631,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
                                 if (j >= nval) break;
-                                a.y[(size_t)(t.p0 + c0 + j) * a.N + t.rt * kTileRows + r] =
+                                a.y[(size_t)(t.p0 + c0 + j) * a.N + rt * kTileRows + r] =
                                     __uint_as_float(v[j]);
                             }
                         }
@@ -574,7 +647,18 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&sm->acc_empty[acc]);
+            if (kPair) {
+                // one arrival per warp, on the even CTA's barrier
+                __syncwarp();
+                if (lane == 0) {
+                    if (rank == 0)
+                        mbar_arrive(&sm->acc_empty[acc]);
+                    else
+                        mbar_arrive_remote(&sm->acc_empty[acc], 0);
+                }
+            } else {
+                mbar_arrive(&sm->acc_empty[acc]);
+            }
 
             if (!whole) {
                 // Fixed-order reduction by whichever CTA finishes the tile
@@ -620,19 +704,27 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     // ---------------- teardown
     tc_fence_before();
     __syncthreads();
+    // no arrival of one CTA of a pair may reach the other after it exits
+    if (kPair) cluster_sync();
     if (warp == kMmaWarp) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tb, kTmemCols);
+        if (kPair)
+            tmem_dealloc_pair(tb, kTmemCols);
+        else
+            tmem_dealloc(tb, kTmemCols);
     }
 }
 
 using KernelFn = void (*)(const TcArgs, const CUtensorMap);
 
-template <int KIND, int NT>
+template <int KIND, int NT, int CG = 1>
 struct Config {
-    static constexpr int kTokBoxes = (KIND == MOE_PACK_W2) ? 4 : 2;
-    static constexpr int kStage = kTokBoxes * NT * 128 + kBlockBytes;
+    // (CTA pairs: this CTA's half of the token operand per stage)
+    static constexpr bool kPair = CG == 2;
+    static constexpr int kTokRows = (kPair && KIND == MOE_PACK_W13) ? NT / 2 : NT;
+    static constexpr int kTokBoxes = (KIND == MOE_PACK_W2 && !kPair) ? 4 : 2;
+    static constexpr int kStage = kTokBoxes * kTokRows * 128 + kBlockBytes;
     static constexpr int kBudget = 210 * 1024;
     // An even stage count keeps every shared-memory stage with one dequant
     // warpgroup (chunk c and chunk c + kStages have the same parity), so a
@@ -675,24 +767,33 @@ struct Config {
     static constexpr size_t kMinSmem = 120 * 1024;
     static constexpr size_t kNeed = (size_t)kStages * kStage + sizeof(Smem) + 1024;
     static constexpr size_t kSmem = kNeed > kMinSmem ? kNeed : kMinSmem;
-    static KernelFn fn() { return gemm_tc_kernel<KIND, NT, kStages, kDq, kProd, kMma>; }
+    static KernelFn fn() { return gemm_tc_kernel<KIND, NT, kStages, kDq, kProd, kMma, CG>; }
 };
 
-template <int KIND, int NT>
-bool pick_nt(KernelFn *fn, size_t *smem, int *threads) {
-    *fn = Config<KIND, NT>::fn();
-    *smem = Config<KIND, NT>::kSmem;
-    *threads = Config<KIND, NT>::kThreads;
+template <int KIND, int NT, int CG>
+bool pick_cfg(KernelFn *fn, size_t *smem, int *threads) {
+    *fn = Config<KIND, NT, CG>::fn();
+    *smem = Config<KIND, NT, CG>::kSmem;
+    *threads = Config<KIND, NT, CG>::kThreads;
     return true;
 }
 
+// (the CTA-pair kernels exist for the tile widths tc_pair_mode names)
+template <int KIND, int NT>
+bool pick_nt(bool pair, KernelFn *fn, size_t *smem, int *threads) {
+    if constexpr ((KIND == MOE_PACK_W13 && NT == 128) || (KIND == MOE_PACK_W2 && NT == 64)) {
+        if (pair) return pick_cfg<KIND, NT, 2>(fn, smem, threads);
+    }
+    return pick_cfg<KIND, NT, 1>(fn, smem, threads);
+}
+
 template <int KIND>
-bool pick(int nt, KernelFn *fn, size_t *smem, int *threads) {
+bool pick(int nt, bool pair, KernelFn *fn, size_t *smem, int *threads) {
     switch (nt) {
-        case 16: return pick_nt<KIND, 16>(fn, smem, threads);
-        case 32: return pick_nt<KIND, 32>(fn, smem, threads);
-        case 64: return pick_nt<KIND, 64>(fn, smem, threads);
-        case 128: return pick_nt<KIND, 128>(fn, smem, threads);
+        case 16: return pick_nt<KIND, 16>(pair, fn, smem, threads);
+        case 32: return pick_nt<KIND, 32>(pair, fn, smem, threads);
+        case 64: return pick_nt<KIND, 64>(pair, fn, smem, threads);
+        case 128: return pick_nt<KIND, 128>(pair, fn, smem, threads);
     }
     return false;
 }
@@ -735,7 +836,7 @@ bool make_token_map(CUtensorMap *map, const void *ptr, int rows, int cols, int b
 }
 
 bool make_act_map(CUtensorMap *map, const void *hi, const void *lo, int rows, int cols,
-                  int box_rows, bool stacked) {
+                  int box_rows, bool stacked, bool one_half) {
     EncodeTiledFn enc = encoder();
     if (!enc) return false;
     const uintptr_t h = reinterpret_cast<uintptr_t>(hi), l = reinterpret_cast<uintptr_t>(lo);
@@ -745,7 +846,7 @@ bool make_act_map(CUtensorMap *map, const void *hi, const void *lo, int rows, in
     // dimension 0: 64 columns; 1: rows; then (hi/lo, K half) or (K half, hi/lo)
     cuuint64_t dims[4] = {64, r, stacked ? 2 : kh, stacked ? kh : 2};
     cuuint64_t strides[3] = {row_b, stacked ? half_b : 128, stacked ? 128 : half_b};
-    cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 2, 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_rows, (one_half && stacked) ? 1u : 2u, 2};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void *>(hi), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -772,9 +873,13 @@ cudaError_t launch_gemm_tc(const TcArgs &args, const CUtensorMap &tok, int grid,
     KernelFn fn = nullptr;
     size_t smem = 0;
     int threads = 0;
-    const bool ok = (args.kind == MOE_PACK_W13) ? pick<MOE_PACK_W13>(args.nt, &fn, &smem, &threads)
-                                                : pick<MOE_PACK_W2>(args.nt, &fn, &smem, &threads);
+    const bool pair = tc_pair_mode(args.kind, args.nt, args.N);
+    const bool ok = (args.kind == MOE_PACK_W13)
+                        ? pick<MOE_PACK_W13>(args.nt, pair, &fn, &smem, &threads)
+                        : pick<MOE_PACK_W2>(args.nt, pair, &fn, &smem, &threads);
     if (!ok) return cudaErrorInvalidValue;
+    if (pair) grid &= ~1;  // whole CTA pairs
+    if (grid < 1) return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
@@ -782,11 +887,22 @@ cudaError_t launch_gemm_tc(const TcArgs &args, const CUtensorMap &tok, int grid,
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n_attr = 0;
+    if (pdl) {
+        attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+        ++n_attr;
+    }
+    if (pair) {
+        attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+        attr[n_attr].val.clusterDim.x = 2;
+        attr[n_attr].val.clusterDim.y = 1;
+        attr[n_attr].val.clusterDim.z = 1;
+        ++n_attr;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = n_attr;
     return cudaLaunchKernelEx(&cfg, fn, args, tok);
 }
 

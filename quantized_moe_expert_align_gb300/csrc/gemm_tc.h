@@ -40,6 +40,20 @@ struct TcArgs {
 // B operand (small token tiles); the kernel and its tensor map agree on it.
 inline bool stacked_hi_lo(int nt) { return nt <= 64; }
 
+// Whether the GEMM of `kind` (MOE_PACK_W13 / W2) with nt-row token tiles over
+// an N-row weight matrix runs on CTA pairs: two SMs share each MMA
+// (tcgen05 cta_group::2, 256 weight rows, 128 in each SM's tensor memory)
+// and each loads only half of the token operand -- half of the token rows
+// (gate+up) or one of the hi / lo halves (down).  That is done where a chunk
+// of token rows is 32 KiB (128-row gate+up tiles, 64-row down tiles), which
+// one SM cannot take in as fast as its tensor core uses it, and needs the
+// 128-row weight tiles of an expert to come in pairs (N a multiple of 256).
+// The kernel choice and the token maps follow it.
+inline bool tc_pair_mode(int kind, int nt, int N) {
+    const bool big = (kind == MOE_PACK_W13) ? nt == 128 : nt == 64;
+    return big && N % (2 * kTileRows) == 0;
+}
+
 // Token operand of the gate+up GEMM: fp16 [rows][cols] (row-major) seen as
 // 3-D (64 columns, rows, cols/64) so that one copy brings a 128-column K
 // chunk of box_rows rows, stored as two 64-column slabs of box_rows x 128 B
@@ -48,9 +62,11 @@ bool make_token_map(CUtensorMap *map, const void *ptr, int rows, int cols, int b
 // Token operand of the down GEMM: the hi and lo fp16 halves of the
 // activation (lo at a fixed byte distance after hi) as one 4-D map, so that
 // one copy brings both halves of a K chunk: slabs in the order
-// [K half][hi, lo] when `stacked`, [hi, lo][K half] otherwise.
+// [K half][hi, lo] when `stacked`, [hi, lo][K half] otherwise.  With
+// `one_half` (CTA pairs, stacked) a copy brings only the hi or only the lo
+// rows (the third coordinate picks which) of both K halves.
 bool make_act_map(CUtensorMap *map, const void *hi, const void *lo, int rows, int cols,
-                  int box_rows, bool stacked);
+                  int box_rows, bool stacked, bool one_half = false);
 int tc_grid(int device);
 cudaError_t launch_gemm_tc(const TcArgs &args, const CUtensorMap &tok, int grid, cudaStream_t s,
                            bool pdl);

@@ -81,6 +81,34 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
         : "memory");
     return ok != 0;
 }
+// ---------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// All threads of every CTA of the cluster; release / acquire at cluster scope.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+// Arrive on the mbarrier at the same shared-memory offset in CTA `rank` of
+// the cluster, with the default semantics of an arrive (release, CTA
+// scope), as on a local barrier.  What the other CTA must see is ordered by
+// the tcgen05 fences around the arrive and the wait (tensor-memory stores
+// completed by tcgen05.wait::st, reads by tcgen05.wait::ld) and by the
+// copies' own barriers; a release at cluster scope here held each arrive
+// back until the SM's outstanding memory operations had completed (about a
+// microsecond with copies in flight).
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t *bar, uint32_t rank) {
+    asm volatile(
+        "{\n\t.reg .b32 ra;\n\t"
+        "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+        "mbarrier.arrive.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar)),
+        "r"(rank)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
@@ -144,6 +172,21 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                  : "memory");
 }
+// The same for a CTA pair (cta_group::2): one warp of each CTA of the pair
+// executes them; both CTAs get the same tensor-memory address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -155,6 +198,14 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
+        : "memory");
+}
+// For pair MMAs: arrive on the mbarrier at `bar`'s offset in both CTAs of the pair.
+__device__ __forceinline__ void tc_commit_pair(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(smem_u32(bar)),
+        "h"((uint16_t)3)
         : "memory");
 }
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -184,14 +235,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 }
 
 // Instruction descriptor, kind::f16: fp16 A and B, fp32 D, both K-major,
-// M = 128, N in [16, 256] with N % 16 == 0.
-__host__ __device__ constexpr uint32_t idesc_f16_m128(uint32_t n) {
+// M = 128 (one CTA) or 256 (a CTA pair), N in [16, 256] with N % 16 == 0.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t m, uint32_t n) {
     return (1u << 4)              // D format: f32
            | (0u << 7)            // A format: f16
            | (0u << 10)           // B format: f16
            | ((n >> 3) << 17)     // N >> 3
-           | ((128u >> 4) << 24); // M >> 4
+           | ((m >> 4) << 24);    // M >> 4
 }
+__host__ __device__ constexpr uint32_t idesc_f16_m128(uint32_t n) { return idesc_f16(128, n); }
 
 // Shared-memory matrix descriptor for a K-major operand stored as TMA writes
 // it with 128-byte swizzling: rows of 128 bytes, 8-row groups 1024 bytes
@@ -214,6 +266,19 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// The same over a CTA pair (M = 256), issued by one thread of the even CTA:
+// each CTA's tensor memory holds its 128 rows of A and of D (all N columns
+// of D), and B's rows (the N side) are split in two halves, the first in the
+// even CTA's shared memory, the second at the same offset in the odd one's.
+__device__ __forceinline__ void mma_f16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }

@@ -2,8 +2,11 @@
 library takes (1024, with enough tiles for the round-robin whole-tile
 schedule), every expert selected (k = E = 64), odd tile and chunk counts
 (H = 384: three 128-row tiles of the down GEMM and three K chunks of the
-gate+up GEMM; I = 128: one K chunk of the down GEMM), and the 128-row token
-tile of the down GEMM, which the library only picks when told to."""
+gate+up GEMM; I = 128: one K chunk of the down GEMM), the 128-row token
+tile of the down GEMM, which the library only picks when told to, and the
+CTA-pair kernels (128-row gate+up and 64-row down token tiles) on experts
+of every ragged row count, next to a down GEMM whose odd number of weight
+tiles keeps it on single CTAs."""
 import json
 import os
 import subprocess
@@ -31,6 +34,43 @@ def _run(L, M, seed=0):
     what = f"E{L.E} H{L.H} I{L.I} k{L.k} M{M}"
     ref, _ = gu.check_stages(dl, x, ids, w, ws.buf, np.arange(M * L.k), what)
     return gu.parity(gu.bf16_dev_to_f64(out), ref["out"], what)
+
+
+def _run_counts(L, counts, seed=0):
+    """k = 1, expert e routed exactly counts[e] tokens (in a shuffled order),
+    all routing weights 1; every token's output and every slot's act and y."""
+    import quantized_moe_expert_align_gb300 as moe
+    rng = np.random.default_rng(seed)
+    ids = np.repeat(np.arange(L.E, dtype=np.int32), counts)
+    ids = ids[rng.permutation(ids.size)].reshape(-1, 1)
+    M = ids.shape[0]
+    w = np.ones((M, 1), np.float32)
+    dl = gu.DeviceLayer(L, seed)
+    x = synth.hidden(M, L.H, seed)
+    out, ws = dl.forward(x, ids, w)
+    st, _ = moe.moe_w4a16_get_device_status(ws.buf)
+    assert st == moe.MOE_OK, moe.moe_status_string(st)
+    what = f"E{L.E} H{L.H} I{L.I} counts {list(counts)}"
+    ref, _ = gu.check_stages(dl, x, ids, w, ws.buf, np.arange(M), what)
+    gu.parity(gu.bf16_dev_to_f64(out), ref["out"], what)
+    return moe.moe_w4a16_get_diag()["token_tile"]
+
+
+# rows per expert around every multiple of 16 and 32 up to two 128-row tiles
+_RAGGED = [1, 15, 16, 17, 31, 33, 47, 48, 63, 64, 65, 95, 97, 127, 128, 129, 160, 200, 255, 256]
+
+
+def test_cta_pairs_ragged_tiles(gpu):
+    """Both GEMMs on CTA pairs (4 and 2 weight tiles per expert): gate+up
+    token tiles whose rows round up to 32, 64, 96 or 128 MMA columns (half
+    of them in each CTA), down tiles of 1-64 rows."""
+    assert _run_counts(synth.Layer(20, 256, 256, 1), _RAGGED) == 128
+
+
+def test_cta_pairs_next_to_single_ctas(gpu):
+    """H = 384: the down GEMM's three weight tiles per expert keep it on
+    single CTAs (64-row token tiles) while the gate+up GEMM runs on pairs."""
+    assert _run_counts(synth.Layer(20, 384, 128, 1), _RAGGED[::-1], seed=1) == 128
 
 
 def test_e1024_round_robin(gpu):
