@@ -57,10 +57,10 @@ FUSED_KERNEL = "decode_fused"   # opt-in: the whole layer in one kernel
 # longer describes the kernel and the bench reports traffic as null.
 TRAFFIC_CAPTURE = {
     "kernel": "gemm_gate_up",
-    "sources_sha256": "238f10eda9f2b2fd8387b618e8edfe3c5874b7f091e3dc6337f5aca375aaf543",
+    "sources_sha256": "08946c9afcf7aef936145e2b4fb72831642d6ef8c1ef16498b77091043d7f05c",
     "workload": "decode_e384_h7168_i2048_top8",
-    "bytes_per_launch": {1: 132318464 + 2811648, 9: 1091240704 + 519168,
-                         90: 5559526400 + 2526976},
+    "bytes_per_launch": {1: 132322560 + 2793216, 9: 1091147008 + 502272,
+                         90: 5559594752 + 2114560},
     "profile": "profiles/dram_gemm_gate_up_decode_e384_m1_9_90.md",
 }
 KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "tc_common.cuh", "sm100.cuh", "moe_internal.h",

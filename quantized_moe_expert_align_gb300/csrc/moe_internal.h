@@ -140,9 +140,12 @@ struct AlignArgs {
 };
 cudaError_t launch_align(const AlignArgs &a, cudaStream_t s);
 // Batches of more than kAlignLargeSlots slots are aligned by kAlignSegs CTAs
-// (three kernels) instead of one.
+// (three kernels) instead of one.  One CTA's time grows with the slots it
+// walks (13 us at 2048 slots, 25 at 8192, 42 at 16384 on one GB300); the
+// three kernels take 13-15 us at 8192-16384 slots and 17 at 32768, so the
+// switch is at 2048 (E = 128 M = 2048: 893 -> 866 us per layer call).
 constexpr int kAlignSegs = 32;
-constexpr int kAlignLargeSlots = 1 << 14;
+constexpr int kAlignLargeSlots = 2048;
 inline bool align_large(int64_t n) { return n > kAlignLargeSlots; }
 
 // Router front-end: topk ids / weights from fp32 logits, one warp per token.

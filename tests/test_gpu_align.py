@@ -53,7 +53,7 @@ def test_align_edge_cases(gpu):
                    (rng.integers(0, 4, size=(77, 6)), 4), (np.zeros((50, 2)), 1),
                    (rng.integers(0, 1024, size=(999, 8)), 1024),
                    (rng.integers(0, 384, size=(16384, 8)), 384),
-                   (rng.integers(0, 384, size=(2048, 8)), 384),     # the one-CTA maximum
+                   (rng.integers(0, 384, size=(256, 8)), 384),      # the one-CTA maximum
                    (rng.integers(0, 5, size=(1111, 3)), 5)]:
         st, _, bad = _check(np.asarray(ids, np.int32), E)
         assert st == moe.MOE_OK and bad == 0
@@ -79,12 +79,13 @@ def test_align_out_of_range_ids(gpu):
 
 
 def test_align_large_batches(gpu):
-    """More than 16384 slots take the multi-CTA path (per-segment counts,
+    """More than 2048 slots take the multi-CTA path (per-segment counts,
     one scan, per-segment placement): still the same stable counting sort,
     out-of-range ids included."""
     import quantized_moe_expert_align_gb300 as moe
     rng = np.random.default_rng(11)
-    for ids, E in [(rng.integers(0, 384, size=(16385, 1)), 384),      # just above the switch
+    for ids, E in [(rng.integers(0, 384, size=(2049, 1)), 384),       # just above the switch
+                   (rng.integers(0, 384, size=(16385, 1)), 384),
                    (rng.integers(0, 1024, size=(3000, 8)), 1024),
                    (np.zeros((5000, 4)), 1),
                    (np.full((2100, 8), 17), 64),                      # one expert takes all

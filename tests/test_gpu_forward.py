@@ -126,7 +126,7 @@ def test_wide_and_zero_scales(gpu, which):
     gu.parity(gu.bf16_dev_to_f64(out), dl.oracle(x, ids, w), f"wide scale in {which}")
 
 
-# ---- Zipf prefill: the 32-CTA alignment (more than 16384 slots), 128-row
+# ---- Zipf prefill: the 32-CTA alignment (more than 2048 slots), 128-row
 # token tiles, experts spanning many token tiles
 @pytest.mark.parametrize("M,heavy_full", [(4096, 1), (16384, 0)])
 def test_prefill_zipf_e384(e384_layer, M, heavy_full):
