@@ -10,7 +10,10 @@ from tests import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("wl,M", [(synth.TOY, 4), (synth.SECOND, 1), (synth.SECOND, 32)])
+# (M = 2048: the 32-CTA alignment and both GEMMs on CTA pairs, cluster launches
+# inside the captured graph)
+@pytest.mark.parametrize("wl,M", [(synth.TOY, 4), (synth.SECOND, 1), (synth.SECOND, 32),
+                                  (synth.SECOND, 2048)])
 def test_forward_in_cuda_graph(request, wl, M):
     import quantized_moe_expert_align_gb300 as moe
     torch = gu.torch_mod()
