@@ -16,11 +16,11 @@ namespace moe {
 constexpr int kMaxGrid = 256;  // bound on the GEMM grid used to size workspaces
 
 int pick_token_tile(int n, int E) {
-    // Test override: MOE_W4A16_TOKEN_TILE = 16, 32, 64 or 128.
+    // Test override: MOE_W4A16_TOKEN_TILE = 16, 32, 64, 128 or 160.
     static const int forced = [] {
         const char *v = std::getenv("MOE_W4A16_TOKEN_TILE");
         const int t = v ? std::atoi(v) : 0;
-        return (t == 16 || t == 32 || t == 64 || t == 128) ? t : 0;
+        return (t == 16 || t == 32 || t == 64 || t == 128 || t == 160) ? t : 0;
     }();
     if (forced) return forced;
     // Rows per active expert if routing spreads the slots evenly.  The tile
@@ -36,6 +36,11 @@ int pick_token_tile(int n, int E) {
     const int want = avg + avg / 4;
     int nt = 16;
     while (nt < want && nt < 128) nt <<= 1;
+    // Beyond 128 rows the gate+up GEMM takes 160-row tiles (on CTA pairs,
+    // 80 rows in each SM): at E = 128 M = 2048 (128 +- 11 rows per expert)
+    // a third of the 128-row tiles were second tiles of a few rows, each
+    // dequantising the expert's whole weight tile for a narrow MMA.
+    if (nt == 128 && want > 128) nt = 160;
     return nt;
 }
 

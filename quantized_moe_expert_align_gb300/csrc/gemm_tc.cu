@@ -69,6 +69,11 @@ __host__ __device__ constexpr int threads_for(int dq_groups, int producers, int 
     return 32 * (kEpiWarps + 4 * dq_groups + producers + mma_warps);
 }
 constexpr int kMaxABufs = 6;                  // TMEM A buffers (64 columns each)
+// TMEM A buffers of a configuration: one per dequant group, at least four
+// (160-row token tiles: three, next to two 160-column accumulators).
+__host__ __device__ constexpr int a_buffers(int nt, int stages, int dq) {
+    return nt == 160 ? 3 : (stages >= 4 ? (dq > 4 ? dq : 4) : 2);
+}
 constexpr int kACols = kChunkK / 2;           // 64 fp16 pairs per row per chunk
 constexpr uint32_t kTmemCols = 512;
 
@@ -143,8 +148,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     // into one B operand of 2*NT rows, so one MMA (whose cost does not grow
     // with N up to 128) covers both; the epilogue adds the two halves.
     constexpr bool kCat = (KIND == MOE_PACK_W2) && (NT <= 64);  // == stacked_hi_lo(NT)
-    // TMEM A buffers in use (same rule as Config::kAB)
-    constexpr int kAB = (STAGES >= 4) ? (DQG > 4 ? DQG : 4) : 2;
+    constexpr int kAB = a_buffers(NT, STAGES, DQG);  // TMEM A buffers in use
     constexpr int kAccBase = kAB * kACols;
     constexpr int kAccCols = kCat ? 2 * NT : NT;              // columns per accumulator
     static_assert(kAccBase + 2 * MMAW * kAccCols <= 512, "tensor memory budget");
@@ -737,7 +741,10 @@ struct Config {
     // more of the time (decode M = 90: 1026 -> 976 us); the down GEMM, whose
     // epilogue needs more registers, spilled at 64 and stays at 4 groups.
     static constexpr bool kWide = KIND == MOE_PACK_W13 && NT <= 32 && kFit >= 12;
-    static constexpr int kStages = kWide ? 12 : (kFit & ~1);
+    // 160-row gate+up tiles (CTA pairs): 6 stages of 29 KiB, 3 dequant
+    // warpgroups, whose 3 A buffers leave room for the two accumulators
+    static constexpr bool k160 = NT == 160;
+    static constexpr int kStages = kWide ? 12 : (k160 ? 6 : (kFit & ~1));
     // Warp roles.  Each mbarrier wait costs a shared-memory round trip of
     // over a hundred cycles even when the phase is complete, and every
     // instruction of the small control loops waits behind the dequantisation
@@ -750,8 +757,8 @@ struct Config {
     //  * two MMA issuers where N is small enough for the issue rate of
     //    tcgen05.mma, not the tensor pipe, to limit, and their
     //    accumulators fit next to the A buffers in tensor memory.
-    static constexpr int kDq = kWide ? 6 : ((kStages % 4 == 0) ? 4 : 2);
-    static constexpr int kAB = kStages >= 4 ? (kDq > 4 ? kDq : 4) : 2;
+    static constexpr int kDq = kWide ? 6 : (k160 ? 3 : ((kStages % 4 == 0) ? 4 : 2));
+    static constexpr int kAB = a_buffers(NT, kStages, kDq);
     static constexpr int kAccCols = (KIND == MOE_PACK_W2 && NT <= 64) ? 2 * NT : NT;
     // (two issuers need the A buffers and stages to split evenly between them)
     static constexpr int kMma = (kAccCols <= 64 && kAB * kACols + 4 * kAccCols <= (int)kTmemCols &&
@@ -781,7 +788,7 @@ bool pick_cfg(KernelFn *fn, size_t *smem, int *threads) {
 // (the CTA-pair kernels exist for the tile widths tc_pair_mode names)
 template <int KIND, int NT>
 bool pick_nt(bool pair, KernelFn *fn, size_t *smem, int *threads) {
-    if constexpr ((KIND == MOE_PACK_W13 && NT == 128) || (KIND == MOE_PACK_W2 && NT == 64)) {
+    if constexpr ((KIND == MOE_PACK_W13 && NT >= 128) || (KIND == MOE_PACK_W2 && NT == 64)) {
         if (pair) return pick_cfg<KIND, NT, 2>(fn, smem, threads);
     }
     return pick_cfg<KIND, NT, 1>(fn, smem, threads);
@@ -794,6 +801,11 @@ bool pick(int nt, bool pair, KernelFn *fn, size_t *smem, int *threads) {
         case 32: return pick_nt<KIND, 32>(pair, fn, smem, threads);
         case 64: return pick_nt<KIND, 64>(pair, fn, smem, threads);
         case 128: return pick_nt<KIND, 128>(pair, fn, smem, threads);
+        case 160:  // gate+up only, always on CTA pairs
+            if constexpr (KIND == MOE_PACK_W13) {
+                if (pair) return pick_cfg<KIND, 160, 2>(fn, smem, threads);
+            }
+            return false;
     }
     return false;
 }

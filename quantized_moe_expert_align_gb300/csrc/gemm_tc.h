@@ -50,7 +50,7 @@ inline bool stacked_hi_lo(int nt) { return nt <= 64; }
 // 128-row weight tiles of an expert to come in pairs (N a multiple of 256).
 // The kernel choice and the token maps follow it.
 inline bool tc_pair_mode(int kind, int nt, int N) {
-    const bool big = (kind == MOE_PACK_W13) ? nt == 128 : nt == 64;
+    const bool big = (kind == MOE_PACK_W13) ? nt >= 128 : nt == 64;
     return big && N % (2 * kTileRows) == 0;
 }
 

@@ -58,12 +58,12 @@ def test_decode_e384(e384_layer, M):
 
 @pytest.mark.parametrize("M", [1, 32, 256, 2048])
 def test_second_shape(e128_layer, M):
-    """M = 2048: 128-row token tiles of the gate+up GEMM (64 for the down
+    """M = 2048: 160-row token tiles of the gate+up GEMM (64 for the down
     GEMM), round-robin whole tiles."""
     import quantized_moe_expert_align_gb300 as moe
     _full(e128_layer, synth.SECOND, M)
     if M == 2048:
-        assert moe.moe_w4a16_get_diag()["token_tile"] == 128
+        assert moe.moe_w4a16_get_diag()["token_tile"] == 160
 
 
 @pytest.mark.parametrize("M", [256, 512, 1024])
@@ -126,17 +126,17 @@ def test_wide_and_zero_scales(gpu, which):
     gu.parity(gu.bf16_dev_to_f64(out), dl.oracle(x, ids, w), f"wide scale in {which}")
 
 
-# ---- Zipf prefill: the 32-CTA alignment (more than 2048 slots), 128-row
-# token tiles, experts spanning many token tiles
-@pytest.mark.parametrize("M,heavy_full", [(4096, 1), (16384, 0)])
-def test_prefill_zipf_e384(e384_layer, M, heavy_full):
+# ---- Zipf prefill: the 32-CTA alignment (more than 2048 slots), 128- and
+# 160-row token tiles, experts spanning many token tiles
+@pytest.mark.parametrize("M,heavy_full,tile", [(4096, 1, 128), (16384, 0, 160)])
+def test_prefill_zipf_e384(e384_layer, M, heavy_full, tile):
     import quantized_moe_expert_align_gb300 as moe
     wl = synth.PREFILL
     L = wl.layer
     x, ids, w = _inputs(wl, M)
     out, ws = _forward_ok(e384_layer, x, ids, w)
     nt = moe.moe_w4a16_get_diag()["token_tile"]
-    assert nt == 128
+    assert nt == tile
     slots = gu.tile_sample(ids, L.E, nt, gu.down_tile(nt), heavy_full=heavy_full)
     gu.check_stages(e384_layer, x, ids, w, ws.buf, slots, f"{wl.name} M={M}")
     # output rows of sampled tokens (each depends only on its own row, ids

@@ -4,9 +4,9 @@ schedule), every expert selected (k = E = 64), odd tile and chunk counts
 (H = 384: three 128-row tiles of the down GEMM and three K chunks of the
 gate+up GEMM; I = 128: one K chunk of the down GEMM), the 128-row token
 tile of the down GEMM, which the library only picks when told to, and the
-CTA-pair kernels (128-row gate+up and 64-row down token tiles) on experts
-of every ragged row count, next to a down GEMM whose odd number of weight
-tiles keeps it on single CTAs."""
+CTA-pair kernels (128- and 160-row gate+up and 64-row down token tiles) on
+experts of every ragged row count, next to a down GEMM whose odd number of
+weight tiles keeps it on single CTAs."""
 import json
 import os
 import subprocess
@@ -71,6 +71,18 @@ def test_cta_pairs_next_to_single_ctas(gpu):
     """H = 384: the down GEMM's three weight tiles per expert keep it on
     single CTAs (64-row token tiles) while the gate+up GEMM runs on pairs."""
     assert _run_counts(synth.Layer(20, 384, 128, 1), _RAGGED[::-1], seed=1) == 128
+
+
+# rows per expert around every multiple of 32 up to two 160-row tiles, with
+# enough rows on average (about 128) for 160-row gate+up tiles
+_RAGGED_160 = [1, 31, 33, 95, 97, 127, 128, 129, 140, 152, 159, 160, 161, 175, 190, 200,
+               250, 300, 319, 320]
+
+
+def test_cta_pairs_160_row_tiles(gpu):
+    """160-row gate+up tiles (80 rows in each CTA of a pair, MMAs of 32-160
+    columns) and 64-row down tiles."""
+    assert _run_counts(synth.Layer(20, 256, 256, 1), _RAGGED_160, seed=2) == 160
 
 
 def test_e1024_round_robin(gpu):
