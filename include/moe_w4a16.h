@@ -321,14 +321,16 @@ moe_status_t moe_w4a16_workspace_views(int M, int k, int E, int H, int I,
  * calls.
  */
 typedef struct {
-    int32_t version;          /* 1 */
+    int32_t version;          /* 2 */
     int32_t M, k, E, H, I;
-    int32_t token_tile;       /* token rows per MMA tile (the MMA N extent) */
+    int32_t token_tile;       /* token rows per tile of the gate+up GEMM */
     int32_t grid_gemm1;       /* CTAs of the gate+up GEMM */
     int32_t grid_gemm2;       /* CTAs of the down GEMM */
     int32_t kernels_launched; /* kernels one forward call launches */
     int64_t workspace_bytes;  /* bytes of workspace the call used */
     int64_t calls;            /* forward calls since load */
+    int32_t token_tile2;      /* token rows per tile of the down GEMM (version 2) */
+    int32_t reserved;         /* 0 */
 } moe_diag_t;
 
 moe_status_t moe_w4a16_get_diag(moe_diag_t *diag);

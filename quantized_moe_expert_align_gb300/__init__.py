@@ -49,7 +49,8 @@ class moe_diag_t(ctypes.Structure):
                 ("E", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
                 ("token_tile", ctypes.c_int32), ("grid_gemm1", ctypes.c_int32),
                 ("grid_gemm2", ctypes.c_int32), ("kernels_launched", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_int64), ("calls", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("calls", ctypes.c_int64),
+                ("token_tile2", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _lock = threading.Lock()

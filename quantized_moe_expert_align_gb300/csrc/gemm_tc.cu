@@ -70,9 +70,10 @@ __host__ __device__ constexpr int threads_for(int dq_groups, int producers, int 
 }
 constexpr int kMaxABufs = 6;                  // TMEM A buffers (64 columns each)
 // TMEM A buffers of a configuration: one per dequant group, at least four
-// (160-row token tiles: three, next to two 160-column accumulators).
+// (160-column accumulators -- 160-row gate+up tiles, 80-row down tiles with
+// hi and lo stacked: three, next to two accumulators).
 __host__ __device__ constexpr int a_buffers(int nt, int stages, int dq) {
-    return nt == 160 ? 3 : (stages >= 4 ? (dq > 4 ? dq : 4) : 2);
+    return (nt == 160 || nt == 80) ? 3 : (stages >= 4 ? (dq > 4 ? dq : 4) : 2);
 }
 constexpr int kACols = kChunkK / 2;           // 64 fp16 pairs per row per chunk
 constexpr uint32_t kTmemCols = 512;
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     // Down GEMM with small token tiles: the hi and lo rows of a are stacked
     // into one B operand of 2*NT rows, so one MMA (whose cost does not grow
     // with N up to 128) covers both; the epilogue adds the two halves.
-    constexpr bool kCat = (KIND == MOE_PACK_W2) && (NT <= 64);  // == stacked_hi_lo(NT)
+    constexpr bool kCat = (KIND == MOE_PACK_W2) && (NT <= 64 || NT == 80);  // == stacked_hi_lo(NT)
     constexpr int kAB = a_buffers(NT, STAGES, DQG);  // TMEM A buffers in use
     constexpr int kAccBase = kAB * kACols;
     constexpr int kAccCols = kCat ? 2 * NT : NT;              // columns per accumulator
@@ -741,9 +742,10 @@ struct Config {
     // more of the time (decode M = 90: 1026 -> 976 us); the down GEMM, whose
     // epilogue needs more registers, spilled at 64 and stays at 4 groups.
     static constexpr bool kWide = KIND == MOE_PACK_W13 && NT <= 32 && kFit >= 12;
-    // 160-row gate+up tiles (CTA pairs): 6 stages of 29 KiB, 3 dequant
-    // warpgroups, whose 3 A buffers leave room for the two accumulators
-    static constexpr bool k160 = NT == 160;
+    // 160-column accumulators (160-row gate+up, 80-row down tiles, CTA
+    // pairs): 6 stages of 29 KiB, 3 dequant warpgroups, whose 3 A buffers
+    // leave room for the two accumulators
+    static constexpr bool k160 = NT == 160 || NT == 80;
     static constexpr int kStages = kWide ? 12 : (k160 ? 6 : (kFit & ~1));
     // Warp roles.  Each mbarrier wait costs a shared-memory round trip of
     // over a hundred cycles even when the phase is complete, and every
@@ -759,7 +761,7 @@ struct Config {
     //    accumulators fit next to the A buffers in tensor memory.
     static constexpr int kDq = kWide ? 6 : (k160 ? 3 : ((kStages % 4 == 0) ? 4 : 2));
     static constexpr int kAB = a_buffers(NT, kStages, kDq);
-    static constexpr int kAccCols = (KIND == MOE_PACK_W2 && NT <= 64) ? 2 * NT : NT;
+    static constexpr int kAccCols = (KIND == MOE_PACK_W2 && (NT <= 64 || NT == 80)) ? 2 * NT : NT;
     // (two issuers need the A buffers and stages to split evenly between them)
     static constexpr int kMma = (kAccCols <= 64 && kAB * kACols + 4 * kAccCols <= (int)kTmemCols &&
                                  kAB % 2 == 0 && kStages % 2 == 0)
@@ -801,6 +803,11 @@ bool pick(int nt, bool pair, KernelFn *fn, size_t *smem, int *threads) {
         case 32: return pick_nt<KIND, 32>(pair, fn, smem, threads);
         case 64: return pick_nt<KIND, 64>(pair, fn, smem, threads);
         case 128: return pick_nt<KIND, 128>(pair, fn, smem, threads);
+        case 80:  // down only, always on CTA pairs
+            if constexpr (KIND == MOE_PACK_W2) {
+                if (pair) return pick_cfg<KIND, 80, 2>(fn, smem, threads);
+            }
+            return false;
         case 160:  // gate+up only, always on CTA pairs
             if constexpr (KIND == MOE_PACK_W13) {
                 if (pair) return pick_cfg<KIND, 160, 2>(fn, smem, threads);

@@ -38,7 +38,7 @@ struct TcArgs {
 
 // Whether the down GEMM stacks the hi and lo rows of its activation into one
 // B operand (small token tiles); the kernel and its tensor map agree on it.
-inline bool stacked_hi_lo(int nt) { return nt <= 64; }
+inline bool stacked_hi_lo(int nt) { return nt <= 64 || nt == 80; }
 
 // Whether the GEMM of `kind` (MOE_PACK_W13 / W2) with nt-row token tiles over
 // an N-row weight matrix runs on CTA pairs: two SMs share each MMA
@@ -50,7 +50,7 @@ inline bool stacked_hi_lo(int nt) { return nt <= 64; }
 // 128-row weight tiles of an expert to come in pairs (N a multiple of 256).
 // The kernel choice and the token maps follow it.
 inline bool tc_pair_mode(int kind, int nt, int N) {
-    const bool big = (kind == MOE_PACK_W13) ? nt >= 128 : nt == 64;
+    const bool big = (kind == MOE_PACK_W13) ? nt >= 128 : (nt == 64 || nt == 80);
     return big && N % (2 * kTileRows) == 0;
 }
 

@@ -225,10 +225,3 @@ def tile_sample(ids, E, nt, nt2, heavy_full=1, heavy_edges=4):
         rows.update(range(o, o + min(nt, c)))
         rows.update(range(o + last, o + c))
     return perm[np.array(sorted(rows), np.int64)]
-
-
-def down_tile(nt):
-    """Token rows per tile of the down GEMM for a gate+up tile of ``nt`` rows
-    (the library caps it at 64: its stages hold both halves of the
-    activation)."""
-    return nt if nt <= 64 else 64

@@ -155,6 +155,6 @@ def test_no_gpu_reports_unsupported_device(lib):
     assert _fwd(lib) == moe.MOE_ERR_UNSUPPORTED_DEVICE
 
 
-def test_diag_starts_at_version_1(lib):
+def test_diag_starts_at_version_2(lib):
     d = moe.moe_w4a16_get_diag()
-    assert d["version"] == 1
+    assert d["version"] == 2 and d["reserved"] == 0

@@ -58,12 +58,13 @@ def test_decode_e384(e384_layer, M):
 
 @pytest.mark.parametrize("M", [1, 32, 256, 2048])
 def test_second_shape(e128_layer, M):
-    """M = 2048: 160-row token tiles of the gate+up GEMM (64 for the down
+    """M = 2048: 160-row token tiles of the gate+up GEMM (80 for the down
     GEMM), round-robin whole tiles."""
     import quantized_moe_expert_align_gb300 as moe
     _full(e128_layer, synth.SECOND, M)
     if M == 2048:
-        assert moe.moe_w4a16_get_diag()["token_tile"] == 160
+        d = moe.moe_w4a16_get_diag()
+        assert d["token_tile"] == 160 and d["token_tile2"] == 80
 
 
 @pytest.mark.parametrize("M", [256, 512, 1024])
@@ -135,9 +136,10 @@ def test_prefill_zipf_e384(e384_layer, M, heavy_full, tile):
     L = wl.layer
     x, ids, w = _inputs(wl, M)
     out, ws = _forward_ok(e384_layer, x, ids, w)
-    nt = moe.moe_w4a16_get_diag()["token_tile"]
-    assert nt == tile
-    slots = gu.tile_sample(ids, L.E, nt, gu.down_tile(nt), heavy_full=heavy_full)
+    d = moe.moe_w4a16_get_diag()
+    nt, nt2 = d["token_tile"], d["token_tile2"]
+    assert nt == tile and nt2 == 80
+    slots = gu.tile_sample(ids, L.E, nt, nt2, heavy_full=heavy_full)
     gu.check_stages(e384_layer, x, ids, w, ws.buf, slots, f"{wl.name} M={M}")
     # output rows of sampled tokens (each depends only on its own row, ids
     # and weights)
