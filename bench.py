@@ -57,10 +57,10 @@ FUSED_KERNEL = "decode_fused"   # opt-in: the whole layer in one kernel
 # longer describes the kernel and the bench reports traffic as null.
 TRAFFIC_CAPTURE = {
     "kernel": "gemm_gate_up",
-    "sources_sha256": "08946c9afcf7aef936145e2b4fb72831642d6ef8c1ef16498b77091043d7f05c",
+    "sources_sha256": "3e5c7667decc25c9cb946de0063dfd48f4580a529484e2a13c992c876c9d7165",
     "workload": "decode_e384_h7168_i2048_top8",
-    "bytes_per_launch": {1: 132322560 + 2793216, 9: 1091147008 + 502272,
-                         90: 5559594752 + 2114560},
+    "bytes_per_launch": {1: 132318208 + 2738432, 9: 1091144960 + 482048,
+                         90: 5559655936 + 2166528},
     "profile": "profiles/dram_gemm_gate_up_decode_e384_m1_9_90.md",
 }
 KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "tc_common.cuh", "sm100.cuh", "moe_internal.h",
