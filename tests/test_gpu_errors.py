@@ -82,16 +82,18 @@ import synth
 from tests import gpu_util as gu
 import quantized_moe_expert_align_gb300 as moe
 L = synth.TOY.layer
+M = int(sys.argv[2]) if len(sys.argv) > 2 else 4
 dl = gu.DeviceLayer(L, 0)
-x = synth.hidden(4, L.H, 0)
-ids, w = synth.routing(4, L, 0)
+x = synth.hidden(M, L.H, 0)
+ids, w = synth.routing(M, L, 0)
 t0 = time.time()
 out, ws = dl.forward(x, ids, w)
 st, detail = moe.moe_w4a16_get_device_status(ws.buf)
 secs = time.time() - t0
+tile = moe.moe_w4a16_get_diag()["token_tile"]
 # the context is still usable afterwards
 y = (torch.arange(1024, device="cuda", dtype=torch.float32) * 2).sum().item()
-print(json.dumps({"status": st, "detail": detail, "secs": secs, "y": y}))
+print(json.dumps({"status": st, "detail": detail, "secs": secs, "y": y, "tile": tile}))
 """
 
 
@@ -113,6 +115,30 @@ def test_bounded_wait_runs_out(gpu):
                        capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
     res = json.loads(r.stdout.strip().splitlines()[-1])
+    assert res["status"] == moe.MOE_ERR_DEVICE_TIMEOUT, res
+    assert 1 <= res["detail"] <= 6
+    assert res["y"] == float(sum(2 * i for i in range(1024)))
+    assert res["secs"] < 60
+
+
+def test_bounded_wait_runs_out_cta_pairs(gpu):
+    """The same with the GEMMs on CTA pairs (M = 300 on the toy layer:
+    128-row gate+up and 80-row down tiles): every wait of both CTAs of a
+    pair still gives up, the pair meets at its closing cluster barrier and
+    the context stays usable."""
+    import json
+    import os
+    import subprocess
+    import sys
+
+    import quantized_moe_expert_align_gb300 as moe
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, MOE_W4A16_TEST_NO_COPIES="1")
+    r = subprocess.run([sys.executable, "-c", _STALL_CHILD, root, "300"], env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    assert res["tile"] == 128, res
     assert res["status"] == moe.MOE_ERR_DEVICE_TIMEOUT, res
     assert 1 <= res["detail"] <= 6
     assert res["y"] == float(sum(2 * i for i in range(1024)))
