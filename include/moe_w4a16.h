@@ -183,7 +183,7 @@ size_t moe_w4a16_workspace_size(int M, int k, int E, int H, int I);
  * 0 <= M, M*k < 2^31.  M == 0 returns MOE_OK without launching.
  * The token-tile width (rows of expert-sorted tokens per tensor-core tile) is
  * chosen from M*k/E; for testing, the environment variable
- * MOE_W4A16_TOKEN_TILE = 16, 32, 64 or 128 fixes it (read once per process;
+ * MOE_W4A16_TOKEN_TILE = 16, 32, 64, 128 or 160 fixes it (read once per process;
  * the workspace size follows it).  For testing the failure path only,
  * MOE_W4A16_TEST_NO_COPIES=1 (read once per process) makes the gate+up GEMM
  * issue no copies: its bounded waits give up after about a second, the call
@@ -192,7 +192,12 @@ size_t moe_w4a16_workspace_size(int M, int k, int E, int H, int I);
  * (values beyond fp16 range set MOE_ERR_DEVICE_FP16_RANGE), fp32
  * accumulation, the activation passed to the down GEMM as an fp16 hi+lo pair.
  * Kernels: five (alignment, hidden gather, gate+up GEMM, down GEMM,
- * combine), chained with programmatic dependent launch.  Opt-in:
+ * combine), chained with programmatic dependent launch; four for batches of
+ * at most 128 slots, whose first kernel aligns (in every CTA) and gathers;
+ * seven above 2048 slots, aligned by three kernels over 32 CTAs.  The GEMMs
+ * with 128/160-row (gate+up) and 64/80-row (down) token tiles run on
+ * clusters of two CTAs (tcgen05 cta_group::2) when the matrix's 128-row
+ * weight tiles come in pairs.  Opt-in:
  * MOE_W4A16_DECODE_FUSED=1 (read once per process) runs batches of at most
  * 128 slots (M*k) whose token tile is 16 rows as one cooperative kernel of
  * one CTA per SM (every CTA resident at once; the call fails with
@@ -213,7 +218,9 @@ moe_status_t moe_w4a16_forward(const uint16_t *hidden, const int32_t *topk_ids,
  * them.  Other arguments, limits and the workspace are those of
  * moe_w4a16_forward (same moe_w4a16_workspace_size), plus k <= E.  Bad
  * logits are reported as in moe_route_align; their tokens' output rows are
- * zero.
+ * zero.  Batches of at most 128 slots with E <= 512 are routed inside the
+ * first kernel (every CTA routes the few tokens itself); others by the
+ * alignment kernel (up to 64 tokens) or a router kernel first.
  */
 moe_status_t moe_w4a16_forward_routed(const uint16_t *hidden, const float *logits,
                                       const void *w13, const void *w2, uint16_t *out,

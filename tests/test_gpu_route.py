@@ -147,9 +147,11 @@ def _routed_forward(dl, wl, M, rows=None):
 
 
 def _launches(M, k):
-    """Kernels of a forward from logits: the five kernels, the alignment
-    kernel routing first up to 64 tokens, else a router kernel first."""
-    return 5 if M <= 64 else 6
+    """Kernels of a forward from logits: batches of at most 128 slots run
+    four (the first routes, aligns and gathers in every CTA); larger ones
+    the five kernels, the alignment kernel routing first up to 64 tokens,
+    else a router kernel first."""
+    return 4 if M * k <= 128 else (5 if M <= 64 else 6)
 
 
 def test_forward_routed_toy(toy_layer):
@@ -165,3 +167,43 @@ def test_forward_routed_decode(e384_layer, M):
 
 def test_forward_routed_second_shape(e128_layer):
     _routed_forward(e128_layer, synth.SECOND, 32)
+
+
+def test_forward_routed_small_batch_bad_logit(toy_layer):
+    """A batch of at most 128 slots routed inside the first kernel: a row
+    with a NaN logit gets zero weights and is reported (its index as the
+    detail), the other rows are routed as the oracle routes them."""
+    import oracle
+    import quantized_moe_expert_align_gb300 as moe
+    torch = gu.torch_mod()
+    L = synth.TOY.layer
+    M = 6
+    x = synth.hidden(M, L.H, seed=1)
+    lg = synth.logits(M, L.E, seed=1)
+    lg[2, 5] = np.nan
+    ws = moe.Workspace(M, L.k, L.E, L.H, L.I, "cuda")
+    xd = gu.to_dev(x.view(np.int16)).view(torch.bfloat16)
+    out, ids_d, w_d = moe.forward_routed(xd, gu.to_dev(lg), L.k, toy_layer.p13, toy_layer.p2,
+                                         L.E, L.I, workspace=ws)
+    torch.cuda.synchronize()
+    st, detail = moe.moe_w4a16_get_device_status(ws.buf)
+    assert st == moe.MOE_ERR_DEVICE_BAD_LOGIT and detail == 2
+    assert moe.moe_w4a16_get_diag()["kernels_launched"] == 4
+    ids, w, _ = oracle.route(lg, L.k)
+    assert np.array_equal(ids_d.cpu().numpy(), ids)
+    assert np.all(w_d.cpu().numpy()[2] == 0)
+    ok = [r for r in range(M) if r != 2]
+    d = np.abs(w_d.cpu().numpy()[ok].astype(np.float64) - w[ok])
+    assert np.all(d <= _weight_tol(lg[ok], ids[ok], w[ok]))
+
+
+def test_forward_routed_wide_router_small_batch(gpu):
+    """E = 1024 (32 logits a lane): small batches keep the router kernel
+    ahead of the five kernels."""
+    import oracle
+    import quantized_moe_expert_align_gb300 as moe
+    L = synth.Layer(1024, 256, 128, 8)
+    dl = gu.DeviceLayer(L, 0)
+    wl = synth.Workload("e1024 routed", L, (2,))
+    d = _routed_forward(dl, wl, 2)
+    assert d["kernels_launched"] == 6
