@@ -84,6 +84,7 @@ struct Smem {
     uint64_t a_full[kMaxABufs];     // A buffer written by the dequant warps
     uint64_t acc_full[2], acc_empty[2];
     uint64_t done;
+    uint64_t turn[2];  // CTA pairs: MMA issuer w may issue its next chunk
     uint32_t tmem_base;
     int abort;
     int bad;
@@ -152,7 +153,12 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     constexpr int kAB = a_buffers(NT, STAGES, DQG);  // TMEM A buffers in use
     constexpr int kAccBase = kAB * kACols;
     constexpr int kAccCols = kCat ? 2 * NT : NT;              // columns per accumulator
-    static_assert(kAccBase + 2 * MMAW * kAccCols <= 512, "tensor memory budget");
+    // CTA pairs with two MMA issuers: tensor memory holds one accumulator
+    // pair (double-buffered), not one per issuer, so the issuers take the
+    // chunks in turns and accumulate into the same one (below)
+    constexpr bool kTurns = kPair && MMAW == 2;
+    constexpr int kAccSets = kTurns ? 1 : MMAW;
+    static_assert(kAccBase + 2 * kAccSets * kAccCols <= 512, "tensor memory budget");
     static_assert(STAGES >= kAB, "a stage must outlive its A buffer's reuse distance");
     static_assert(kStageBytes % 1024 == 0, "stage size must keep 1024-byte alignment");
     static_assert(STAGES % kDqGroups == 0, "each stage must belong to one dequant group");
@@ -163,9 +169,11 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     // a_full barrier a whole phase ahead, where the parity test passes early
     // (a down-GEMM build with 5 A buffers and 2 issuers ran into exactly
     // that: its bounded waits gave up and reported MOE_ERR_DEVICE_TIMEOUT).
-    static_assert(kAB % MMAW == 0 && STAGES % MMAW == 0, "each A buffer must belong to one MMA warp");
-    static_assert(!kPair || (MMAW == 1 && (KIND == MOE_PACK_W13 || kCat)),
-                  "CTA pairs: one MMA issuer; the down GEMM's hi and lo rows split between the CTAs");
+    // (Issuers that take turns never run ahead of each other.)
+    static_assert(kTurns || (kAB % MMAW == 0 && STAGES % MMAW == 0),
+                  "each A buffer must belong to one MMA warp");
+    static_assert(!kPair || KIND == MOE_PACK_W13 || kCat,
+                  "CTA pairs: the down GEMM's hi and lo rows split between the CTAs");
     // mbarrier arrivals: every dequant / epilogue thread of this CTA, or, on
     // CTA pairs, one per warp of both CTAs (on the even CTA's barriers)
     constexpr uint32_t kArrive = kPair ? 8u : 128u;
@@ -203,6 +211,8 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             mbar_init(&sm->acc_empty[b], kArrive);
         }
         mbar_init(&sm->done, MMAW);
+        mbar_init(&sm->turn[0], 1);
+        mbar_init(&sm->turn[1], 1);
         sm->abort = 0;
         sm->bad = !header_ok(a.w, KIND, a.E, a.N, a.K);
         sm->wide = reinterpret_cast<const PackHeader *>(a.w)->wide_scales != 0;
@@ -385,12 +395,20 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
         // accumulates into its own accumulator; the epilogue adds the two.
         // A single issuer is limited by the issue rate of tcgen05.mma at
         // small N, not by the tensor pipe, so two of them go about twice
-        // as fast there.
+        // as fast there.  On CTA pairs the two issuers share one
+        // accumulator and take turns: warp mw issues chunk c only after the
+        // other one has issued chunk c - 1 (its arrival on turn[mw], after
+        // a tcgen05 fence, orders those MMAs before these).  The waits and
+        // the loop of one issuer then overlap the other one's MMA issue,
+        // which a single issuer on a pair could not keep up with the
+        // tensor pipe.
         const int mw = warp - kMmaWarp;
         // stage, A buffer and A-buffer phase of this warp's next chunk, kept
-        // incrementally (STAGES and kAB are multiples of MMAW)
+        // incrementally (STAGES and kAB are multiples of MMAW, or the
+        // issuers take turns: a step of MMAW <= kAB chunks wraps b at most
+        // once)
         int s = mw, b = mw;
-        uint32_t bph = 0;
+        uint32_t bph = 0, tph = 0;
         const uint64_t desc_base = sdesc_k_sw128(smem_u32(base));
         int c = 0, seg = 0;  // c: CTA-local index of the segment's first chunk
         bool ok = true;
@@ -406,13 +424,20 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             if (!warp_wait_bar(&sm->acc_empty[acc], ((seg >> 1) & 1) ^ 1, &sm->abort, a.ctrl, 2))
                 break;
             tc_fence_after();
-            const uint32_t d_tmem = tb + kAccBase + (acc * MMAW + mw) * kAccCols;
+            const uint32_t d_tmem = tb + kAccBase + (acc * kAccSets + (kTurns ? 0 : mw)) * kAccCols;
             const int c_end = c + (k1 - k0);
             bool first = true;
             for (int cc = c + ((mw - c % MMAW) + MMAW) % MMAW; cc < c_end; cc += MMAW) {
                 if (!warp_wait_bar(&sm->a_full[b], bph, &sm->abort, a.ctrl, 3)) {
                     ok = false;
                     break;
+                }
+                if (kTurns && cc > 0) {
+                    if (!warp_wait_bar(&sm->turn[mw], tph, &sm->abort, a.ctrl, 3)) {
+                        ok = false;
+                        break;
+                    }
+                    tph ^= 1;
                 }
                 tc_fence_after();
                 if (elect_one()) {
@@ -424,7 +449,9 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                     const uint32_t a_tmem = tb + b * kACols;
 #pragma unroll
                     for (int j = 0; j < kChunkK / 16; ++j) {
-                        const uint32_t acc_flag = (!first || j > 0) ? 1u : 0u;
+                        // (taking turns, the tile's first chunk starts the
+                        // shared accumulator)
+                        const uint32_t acc_flag = (kTurns ? cc != c : !first) || j > 0 ? 1u : 0u;
                         if (kPair) {  // each CTA's stage: its token rows, K 0-63 then 64-127
                             const uint32_t boff = (j >> 2) * kTokBox + (j & 3) * 32;
                             mma_f16_ts_pair(d_tmem, a_tmem + j * 8, desc0 + (boff >> 4), idesc,
@@ -446,6 +473,10 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                         tc_commit_pair(&sm->consumed[s]);
                     else
                         tc_commit(&sm->consumed[s]);
+                    if (kTurns) {
+                        tc_fence_before();
+                        mbar_arrive(&sm->turn[mw ^ 1]);
+                    }
                 }
                 __syncwarp();
                 first = false;
@@ -459,7 +490,8 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             }
             if (!ok) break;
             // an issuer with no chunk in this segment still arrives (its
-            // accumulator is then not read)
+            // accumulator is then not read; taking turns, the commit of
+            // each issuer covers its own MMAs of the shared one)
             if (elect_one()) {
                 if (kPair)
                     tc_commit_pair(&sm->acc_full[acc]);
@@ -575,11 +607,11 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
             if (!warp_wait_bar(&sm->acc_full[acc], (seg >> 1) & 1, &sm->abort, a.ctrl, 6)) break;
             const int rt = t.rt + (int)rank;  // this CTA's weight tile
             tc_fence_after();
-            const uint32_t acc_addr = tb + lane_off + kAccBase + acc * MMAW * kAccCols;
+            const uint32_t acc_addr = tb + lane_off + kAccBase + acc * kAccSets * kAccCols;
             // with two issuers, the second one had a chunk here unless the
             // segment is a single chunk that fell to the first (and vice versa)
             bool has[2] = {true, true};
-            if (MMAW == 2 && k1 - k0 == 1) {
+            if (kAccSets == 2 && k1 - k0 == 1) {
                 has[0] = (c_seg % 2 == 0);
                 has[1] = !has[0];
             }
@@ -597,7 +629,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                 uint32_t v[16];
                 bool any = false;
 #pragma unroll
-                for (int w = 0; w < MMAW; ++w) {
+                for (int w = 0; w < kAccSets; ++w) {
                     if (!has[w]) continue;
                     uint32_t x[16];
                     tmem_ld16(acc_addr + w * kAccCols + c0, x);
@@ -758,14 +790,21 @@ struct Config {
     //  * two TMA producers (each owns every other stage);
     //  * two MMA issuers where N is small enough for the issue rate of
     //    tcgen05.mma, not the tensor pipe, to limit, and their
-    //    accumulators fit next to the A buffers in tensor memory.
+    //    accumulators fit next to the A buffers in tensor memory; for the
+    //    gate+up GEMM on CTA pairs two issuers that take turns on one
+    //    accumulator (E128 M = 2048 gate+up 360 -> 352 us, Zipf prefill
+    //    M = 4096 / 16384 -1% to -5%; on the down GEMM's pairs the extra
+    //    warp cost 1-2%, so it keeps one issuer there).
     static constexpr int kDq = kWide ? 6 : (k160 ? 3 : ((kStages % 4 == 0) ? 4 : 2));
     static constexpr int kAB = a_buffers(NT, kStages, kDq);
     static constexpr int kAccCols = (KIND == MOE_PACK_W2 && (NT <= 64 || NT == 80)) ? 2 * NT : NT;
-    // (two issuers need the A buffers and stages to split evenly between them)
-    static constexpr int kMma = (kAccCols <= 64 && kAB * kACols + 4 * kAccCols <= (int)kTmemCols &&
-                                 kAB % 2 == 0 && kStages % 2 == 0)
-                                    ? 2 : 1;
+    // (two issuers with accumulators of their own need the A buffers and
+    // stages to split evenly between them)
+    static constexpr int kMma = (CG == 2) ? (KIND == MOE_PACK_W13 ? 2 : 1)
+                                          : ((kAccCols <= 64 &&
+                                              kAB * kACols + 4 * kAccCols <= (int)kTmemCols &&
+                                              kAB % 2 == 0 && kStages % 2 == 0)
+                                                 ? 2 : 1);
     static constexpr int kProd = 2;
     static constexpr int kThreads = threads_for(kDq, kProd, kMma);
     static_assert(kStages >= 2 && kStages % kDq == 0, "stage count must be a multiple of the dequant groups");
