@@ -57,10 +57,10 @@ FUSED_KERNEL = "decode_fused"   # opt-in: the whole layer in one kernel
 # longer describes the kernel and the bench reports traffic as null.
 TRAFFIC_CAPTURE = {
     "kernel": "gemm_gate_up",
-    "sources_sha256": "3e5c7667decc25c9cb946de0063dfd48f4580a529484e2a13c992c876c9d7165",
+    "sources_sha256": "c55fc1ed620c3df3e4f49211a32b8ba2c529a00715ef2493568f48710126d196",
     "workload": "decode_e384_h7168_i2048_top8",
-    "bytes_per_launch": {1: 132318208 + 2738432, 9: 1091144960 + 482048,
-                         90: 5559655936 + 2166528},
+    "bytes_per_launch": {1: 132319232 + 3041024, 9: 1091168768 + 474624,
+                         90: 5559633664 + 2257920},
     "profile": "profiles/dram_gemm_gate_up_decode_e384_m1_9_90.md",
 }
 KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "tc_common.cuh", "sm100.cuh", "moe_internal.h",

@@ -218,9 +218,8 @@ moe_status_t moe_w4a16_forward(const uint16_t *hidden, const int32_t *topk_ids,
  * them.  Other arguments, limits and the workspace are those of
  * moe_w4a16_forward (same moe_w4a16_workspace_size), plus k <= E.  Bad
  * logits are reported as in moe_route_align; their tokens' output rows are
- * zero.  Batches of at most 128 slots with E <= 512 are routed inside the
- * first kernel (every CTA routes the few tokens itself); others by the
- * alignment kernel (up to 64 tokens) or a router kernel first.
+ * zero.  Up to 64 tokens (E <= 512) are routed by the alignment kernel
+ * before it aligns, larger batches by a router kernel first.
  */
 moe_status_t moe_w4a16_forward_routed(const uint16_t *hidden, const float *logits,
                                       const void *w13, const void *w2, uint16_t *out,

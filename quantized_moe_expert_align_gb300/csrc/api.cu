@@ -549,14 +549,13 @@ static moe_status_t forward_impl(const uint16_t *hidden, const int32_t *ids, con
         return MOE_OK;
     }
     const bool pdl = (ev == nullptr);
-    if (n <= kSmallAlignSlots && (!logits || route_vpl(E) <= kAlignRouteMaxVpl)) {
-        // Small batch: one kernel (routes from logits and) aligns, in every
-        // CTA, and gathers; then the two GEMMs and the combine.
+    if (!logits && n <= kSmallAlignSlots) {
+        // Small batch: one kernel aligns (in every CTA) and gathers, then the
+        // two GEMMs and the combine.
         const int pg = small_prep_grid(M, H);
         SmallPrepArgs sp = {ids, hidden, M, k, E, H, L.nt, L.nt2, counts, offsets, tile_prefix,
                             tile_prefix2, perm, inv_perm, xs, ctrl, clear,
-                            reinterpret_cast<int32_t *>(ws + L.ovf), logits,
-                            const_cast<int32_t *>(ids), const_cast<float *>(topk_w)};
+                            reinterpret_cast<int32_t *>(ws + L.ovf)};
         g1.ovf = sp.ovf;
         g1.n_ovf = pg;
         g1.tables_after_wait = 1;

@@ -31,13 +31,6 @@ struct SmallPrepArgs {
     Ctrl *ctrl;
     TicketClear clear;         // both GEMMs' split-K tickets
     int32_t *ovf;              // [grid] per-CTA fp16-overflow flags, written every call
-    // Non-null: every CTA first routes the M tokens from these fp32 logits
-    // [M][E] (E <= 32 * kAlignRouteMaxVpl) into shared memory and aligns
-    // those ids; CTA 0 writes them to route_ids / route_w and reports rows
-    // with a NaN or +inf logit.  ids is then unused.
-    const float *logits;
-    int32_t *route_ids;
-    float *route_w;
 };
 int small_prep_grid(int M, int H);
 cudaError_t launch_align_gather_small(const SmallPrepArgs &a, int grid, cudaStream_t s);

@@ -14,11 +14,8 @@
 // it clears the word, then reports out-of-range ids).  A hidden value beyond
 // fp16 range is recorded in this CTA's own overflow slot, which every call
 // writes, and the gate+up GEMM reports it after its launch wait.
-#include <climits>
-
 #include "device_common.cuh"
 #include "elementwise.h"
-#include "route.cuh"
 #include "small_align.cuh"
 
 namespace moe {
@@ -34,9 +31,6 @@ __device__ __forceinline__ uint32_t half_bits(float v) {
 __global__ void __launch_bounds__(kThreads) align_gather_small_kernel(SmallPrepArgs a) {
     __shared__ SmallAlign sa;
     __shared__ int32_t tp[kSmallAlignSlots + 1], tp2[kSmallAlignSlots + 1];
-    __shared__ int32_t r_ids[kSmallAlignSlots];  // routed ids / weights (logits given)
-    __shared__ float r_w[kSmallAlignSlots];
-    __shared__ int first_bad_row;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, g = blockIdx.x, n = a.M * a.k;
     // the next kernel (the gate+up GEMM) may start its set-up; it waits for
@@ -54,23 +48,7 @@ __global__ void __launch_bounds__(kThreads) align_gather_small_kernel(SmallPrepA
     for (int64_t i = gi; i < a.clear.n / 4; i += gthreads)
         reinterpret_cast<int4 *>(a.clear.tickets)[i] = make_int4(0, 0, 0, 0);
 
-    // From logits every CTA routes the few tokens itself (one warp per
-    // token, the router of the alignment kernel), so that it can align
-    // them without waiting for another CTA.
-    const int32_t *ids = a.ids;
-    if (a.logits) {
-        if (tid == 0) first_bad_row = INT_MAX;
-        __syncthreads();
-        const int vpl = route_vpl(a.E);
-        for (int t = warp; t < a.M; t += kThreads / 32) {
-            const bool bad = route_row_any<kAlignRouteMaxVpl>(vpl, a.logits + (size_t)t * a.E, a.E, a.k,
-                                                              lane, r_ids + t * a.k, r_w + t * a.k);
-            if (bad && lane == 0) atomicMin(&first_bad_row, t);
-        }
-        __syncthreads();
-        ids = r_ids;
-    }
-    small_align(&sa, ids, n, a.E);
+    small_align(&sa, a.ids, n, a.E);
     if (g == 0) {
         if (warp == 0) small_tile_prefix(&sa, a.nt, tp, lane);
         if (warp == 1) small_tile_prefix(&sa, a.nt2, tp2, lane);
@@ -90,18 +68,10 @@ __global__ void __launch_bounds__(kThreads) align_gather_small_kernel(SmallPrepA
             a.perm[p] = p < n_valid ? sa.perm[p] : -1;
             if (a.inv_perm) a.inv_perm[p] = sa.inv[p];
         }
-        if (a.logits) {
-            for (int i = tid; i < n; i += kThreads) {
-                a.route_ids[i] = r_ids[i];
-                a.route_w[i] = r_w[i];
-            }
-        }
         if (tid == 0) {
             a.ctrl->status = 0;
             a.ctrl->detail = 0;
             a.ctrl->n_invalid = n - n_valid;
-            if (a.logits && first_bad_row != INT_MAX)
-                set_status(a.ctrl, MOE_ERR_DEVICE_BAD_LOGIT, first_bad_row);
             if (n_valid < n) set_status(a.ctrl, MOE_ERR_DEVICE_BAD_EXPERT_ID, sa.raw[sa.first_bad_slot]);
         }
     }

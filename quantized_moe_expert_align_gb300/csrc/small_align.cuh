@@ -28,14 +28,14 @@ struct SmallAlign {
 };
 
 // Every thread of the block calls it (at least kSmallAlignSlots threads, in
-// whole warps; n <= kSmallAlignSlots).  ids may be in global or shared
-// memory.  Returns after a block barrier with *sa filled in.
+// whole warps; n <= kSmallAlignSlots).  Returns after a block barrier with
+// *sa filled in.
 __device__ __forceinline__ void small_align(SmallAlign *sa, const int32_t *ids, int n, int E) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) sa->first_bad_slot = kSmallAlignSlots;
     int id = -1;
     if (tid < n) {
-        const int raw = ids[tid];
+        const int raw = __ldg(ids + tid);
         id = (raw >= 0 && raw < E) ? raw : -1;
         sa->raw[tid] = raw;
         sa->sid[tid] = id;

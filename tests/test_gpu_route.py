@@ -147,11 +147,9 @@ def _routed_forward(dl, wl, M, rows=None):
 
 
 def _launches(M, k):
-    """Kernels of a forward from logits: batches of at most 128 slots run
-    four (the first routes, aligns and gathers in every CTA); larger ones
-    the five kernels, the alignment kernel routing first up to 64 tokens,
-    else a router kernel first."""
-    return 4 if M * k <= 128 else (5 if M <= 64 else 6)
+    """Kernels of a forward from logits: the five kernels, the alignment
+    kernel routing first up to 64 tokens, else a router kernel first."""
+    return 5 if M <= 64 else 6
 
 
 def test_forward_routed_toy(toy_layer):
@@ -170,9 +168,9 @@ def test_forward_routed_second_shape(e128_layer):
 
 
 def test_forward_routed_small_batch_bad_logit(toy_layer):
-    """A batch of at most 128 slots routed inside the first kernel: a row
-    with a NaN logit gets zero weights and is reported (its index as the
-    detail), the other rows are routed as the oracle routes them."""
+    """A small routed batch (the alignment kernel routes it): a row with a
+    NaN logit gets zero weights and is reported (its index as the detail),
+    the other rows are routed as the oracle routes them."""
     import oracle
     import quantized_moe_expert_align_gb300 as moe
     torch = gu.torch_mod()
@@ -188,7 +186,7 @@ def test_forward_routed_small_batch_bad_logit(toy_layer):
     torch.cuda.synchronize()
     st, detail = moe.moe_w4a16_get_device_status(ws.buf)
     assert st == moe.MOE_ERR_DEVICE_BAD_LOGIT and detail == 2
-    assert moe.moe_w4a16_get_diag()["kernels_launched"] == 4
+    assert moe.moe_w4a16_get_diag()["kernels_launched"] == _launches(M, L.k)
     ids, w, _ = oracle.route(lg, L.k)
     assert np.array_equal(ids_d.cpu().numpy(), ids)
     assert np.all(w_d.cpu().numpy()[2] == 0)
@@ -198,10 +196,8 @@ def test_forward_routed_small_batch_bad_logit(toy_layer):
 
 
 def test_forward_routed_wide_router_small_batch(gpu):
-    """E = 1024 (32 logits a lane): small batches keep the router kernel
-    ahead of the five kernels."""
-    import oracle
-    import quantized_moe_expert_align_gb300 as moe
+    """E = 1024 (32 logits a lane, beyond the alignment kernel's router):
+    small batches run the router kernel ahead of the five kernels."""
     L = synth.Layer(1024, 256, 128, 8)
     dl = gu.DeviceLayer(L, 0)
     wl = synth.Workload("e1024 routed", L, (2,))
