@@ -7,7 +7,9 @@ layer), inputs already resident in HBM, L2 flushed before every call.  The
 headline value is that workload's tokens/s; the same run also times the rest
 of the metric's M range (the plateau M = 256-1024, the Zipf prefill M = 4096
 and 16384, the second layer shape E=128 M = 1-2048) the same way and reports
-each under ``other_workloads``.
+each under ``other_workloads``.  Every row also gives the µs/call with all
+timed calls of its batch size back to back (``us_per_call_alone``), next to
+the step's interleaved calls.
 
   python bench.py [--gpus N] [--steps K] [--warmup W]
                   [--config decode|plateau|prefill|second|toy|e256|group128]
@@ -277,10 +279,12 @@ def reference_arm(args, wl):
     return 0
 
 
-def layer_rows(wl, batches, call_ms, kernel_ms, hbm_peak, tf_peak):
+def layer_rows(wl, batches, call_ms, kernel_ms, hbm_peak, tf_peak, alone_ms=None):
     """Per batch size: µs/call, tokens/s, active experts and the fraction of
     roofline = max(touched experts' weight bytes / HBM copy rate,
-    6·M·k·H·I / dense fp16 peak) over the measured time."""
+    6·M·k·H·I / dense fp16 peak) over the measured time; with ``alone_ms``
+    also the µs/call and fraction of the calls timed one batch size at a
+    time."""
     L = wl.layer
     b13, b2 = expert_bytes(L)
     rows = []
@@ -305,6 +309,9 @@ def layer_rows(wl, batches, call_ms, kernel_ms, hbm_peak, tf_peak):
             "us_per_call_profiled": round(1e3 * float(k_ms.sum()), 2),
             "pages_ms_rtx_pro_6000": PAGES_MS.get(M) if L.E == 384 else None,
         })
+        if alone_ms is not None:
+            rows[-1]["us_per_call_alone"] = round(1e3 * alone_ms[M], 2)
+            rows[-1]["frac_of_roofline_alone"] = round(t_roof_ms / alone_ms[M], 4)
     return rows
 
 
@@ -379,6 +386,11 @@ class Bench:
         torch.cuda.synchronize()
         return {M: [a.elapsed_time(b) for a, b in ev[M]] for M in Ms}
 
+    def timed_alone(self, fn, Ms, steps):
+        """As timed, but all ``steps`` calls of one batch size back to back
+        before the next size (the step interleaves the sizes)."""
+        return {M: self.timed(fn, [M], steps)[M] for M in Ms}
+
     def kernel_times(self, wl, devb, ws, reps):
         """Per M: (mean ms of each library kernel, the path: "five" kernels,
         "small" -- four, one aligning and gathering -- or "one" for the opt-in
@@ -430,12 +442,14 @@ def extra_sweep(bench, wl, args, local, hbm_peak, tf_peak):
     sampler.start()
     time.sleep(0.3)
     ms = bench.timed(call, wl.Ms, args.steps)
+    alone = bench.timed_alone(call, wl.Ms, args.steps)
     clocks = sampler.stop()
     call_ms = {M: float(np.mean(v)) for M, v in ms.items()}
+    alone_ms = {M: float(np.mean(v)) for M, v in alone.items()}
     k_ms, fused = bench.kernel_times(wl, devb, ws, max(3, min(args.steps, 10)))
     bench.check_status(ws, wl.name)
     rows = layer_rows(wl, batches, call_ms, {M: (k_ms[M], fused[M]) for M in wl.Ms}, hbm_peak,
-                      tf_peak)
+                      tf_peak, alone_ms)
     del devb, ws
     torch.cuda.empty_cache()
     return {"workload": wl.name, "E": L.E, "H": L.H, "I": L.I, "k": L.k, "group": L.group,
@@ -485,8 +499,11 @@ def our_arm(args, wl):
     ms = bench.timed(call, wl.Ms, args.steps)
     if world > 1:
         dist.barrier()
+    # (each batch size alone, for the sweep rows; not part of the step)
+    alone = bench.timed_alone(call, wl.Ms, args.steps)
     clocks = sampler.stop()
     call_ms = {M: float(np.mean(v)) for M, v in ms.items()}
+    alone_ms = {M: float(np.mean(v)) for M, v in alone.items()}
     total_ms = max_over_ranks(sum(sum(v) for v in ms.values()), "cuda")
     tokens_per_step = sum(wl.Ms)
     value = job_value(tokens_per_step, args.steps, world, total_ms)
@@ -597,7 +614,7 @@ def our_arm(args, wl):
     # small-batch kernel) -- over its mean launch duration
     b13, b2 = expert_bytes(L)
     sweep = layer_rows(wl, batches, call_ms, {M: (per_kernel[M], fused[M]) for M in wl.Ms},
-                       hbm_peak, tf_peak)
+                       hbm_peak, tf_peak, alone_ms)
     per_name = {}
     for row in sweep:
         M = row["M"]
