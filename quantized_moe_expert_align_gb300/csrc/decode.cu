@@ -101,6 +101,7 @@ struct Smem {
     uint64_t a_full[kAB];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t done;
+    uint32_t dq_magic[2];  // {kMagic16, kMagic1024}, loaded by the dequant warps
     uint32_t tmem_base;
     int abort;
     int bad;                     // a prepacked header does not match
@@ -275,6 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm->acc_empty[b], 128);
         }
         mbar_init(&sm->done, kMmaWarps);
+        sm->dq_magic[0] = kMagic16;
+        sm->dq_magic[1] = kMagic1024;
         sm->abort = 0;
         sm->bad = !header_ok(a.w13, MOE_PACK_W13, a.E, 2 * a.I, a.H) ||
                   !header_ok(a.w2, MOE_PACK_W2, a.E, a.H, a.I);
@@ -605,6 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = (warp & 3) * 32 + lane;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const int my0 = m[0].my;
+        const DqMagic mg = load_dq_magic(sm->dq_magic);
         const bool wide0 = sm->wide[0] != 0, wide1 = sm->wide[1] != 0;
         // stage, its phase and the A buffer of this group's next chunk, kept
         // incrementally (kStages and kAB are multiples of kDqGroups)
@@ -639,13 +643,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __half2 s2 = __halves2half2(hs, hs);
                     const __half2 c2 = kFused ? __hmul2(s2, __floats2half2_rn(-24.f, -24.f)) : s2;
                     uint32_t v[16], o[4];
-                    dequant_word<kFused>(q.x, s2, c2, o);
+                    dequant_word<kFused>(q.x, s2, c2, mg, o);
                     v[0] = o[0]; v[1] = o[1]; v[2] = o[2]; v[3] = o[3];
-                    dequant_word<kFused>(q.y, s2, c2, o);
+                    dequant_word<kFused>(q.y, s2, c2, mg, o);
                     v[4] = o[0]; v[5] = o[1]; v[6] = o[2]; v[7] = o[3];
-                    dequant_word<kFused>(q.z, s2, c2, o);
+                    dequant_word<kFused>(q.z, s2, c2, mg, o);
                     v[8] = o[0]; v[9] = o[1]; v[10] = o[2]; v[11] = o[3];
-                    dequant_word<kFused>(q.w, s2, c2, o);
+                    dequant_word<kFused>(q.w, s2, c2, mg, o);
                     v[12] = o[0]; v[13] = o[1]; v[14] = o[2]; v[15] = o[3];
                     tmem_st16(a_addr + pc * 16, v);
                 }

@@ -85,6 +85,7 @@ struct Smem {
     uint64_t acc_full[2], acc_empty[2];
     uint64_t done;
     uint64_t turn[2];  // CTA pairs: MMA issuer w may issue its next chunk
+    uint32_t dq_magic[2];  // {kMagic16, kMagic1024}, loaded by the dequant warps
     uint32_t tmem_base;
     int abort;
     int bad;
@@ -213,6 +214,8 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
         mbar_init(&sm->done, MMAW);
         mbar_init(&sm->turn[0], 1);
         mbar_init(&sm->turn[1], 1);
+        sm->dq_magic[0] = kMagic16;
+        sm->dq_magic[1] = kMagic1024;
         sm->abort = 0;
         sm->bad = !header_ok(a.w, KIND, a.E, a.N, a.K);
         sm->wide = reinterpret_cast<const PackHeader *>(a.w)->wide_scales != 0;
@@ -517,6 +520,7 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
         const int grp = (warp - kEpiWarps) / 4;
         const bool wide = sm->wide != 0;
         const int r = (warp & 3) * 32 + lane;  // weight row of the tile = TMEM lane
+        const DqMagic mg = load_dq_magic(sm->dq_magic);
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         // stage, its phase and the A buffer of this group's next chunk, kept
         // incrementally (STAGES and kAB are multiples of kDqGroups)
@@ -555,13 +559,13 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
                     const __half2 c2 = kFused ? __hmul2(s2, __floats2half2_rn(-24.f, -24.f)) : s2;
                     uint32_t v[16];
                     uint32_t o[4];
-                    dequant_word<kFused>(q.x, s2, c2, o);
+                    dequant_word<kFused>(q.x, s2, c2, mg, o);
                     v[0] = o[0]; v[1] = o[1]; v[2] = o[2]; v[3] = o[3];
-                    dequant_word<kFused>(q.y, s2, c2, o);
+                    dequant_word<kFused>(q.y, s2, c2, mg, o);
                     v[4] = o[0]; v[5] = o[1]; v[6] = o[2]; v[7] = o[3];
-                    dequant_word<kFused>(q.z, s2, c2, o);
+                    dequant_word<kFused>(q.z, s2, c2, mg, o);
                     v[8] = o[0]; v[9] = o[1]; v[10] = o[2]; v[11] = o[3];
-                    dequant_word<kFused>(q.w, s2, c2, o);
+                    dequant_word<kFused>(q.w, s2, c2, mg, o);
                     v[12] = o[0]; v[13] = o[1]; v[14] = o[2]; v[15] = o[3];
                     tmem_st16(a_addr + pc * 16, v);
                 }
