@@ -59,10 +59,10 @@ FUSED_KERNEL = "decode_fused"   # opt-in: the whole layer in one kernel
 # longer describes the kernel and the bench reports traffic as null.
 TRAFFIC_CAPTURE = {
     "kernel": "gemm_gate_up",
-    "sources_sha256": "c55fc1ed620c3df3e4f49211a32b8ba2c529a00715ef2493568f48710126d196",
+    "sources_sha256": "9275c6c5618209509aad579bd8033ffcccee035f80c42a8467d506015b49eaa9",
     "workload": "decode_e384_h7168_i2048_top8",
-    "bytes_per_launch": {1: 132319232 + 3041024, 9: 1091168768 + 474624,
-                         90: 5559633664 + 2257920},
+    "bytes_per_launch": {1: 132318720 + 2753536, 9: 1091142656 + 563712,
+                         90: 5559584256 + 2228736},
     "profile": "profiles/dram_gemm_gate_up_decode_e384_m1_9_90.md",
 }
 KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "tc_common.cuh", "sm100.cuh", "moe_internal.h",
