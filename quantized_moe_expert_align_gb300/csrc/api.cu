@@ -15,6 +15,12 @@ namespace moe {
 
 constexpr int kMaxGrid = 256;  // bound on the GEMM grid used to size workspaces
 
+// Rows per active expert if routing spreads the n slots evenly (rounded up).
+static int rows_per_active_expert(int64_t n, int E) {
+    const int64_t active = n < E ? (n > 0 ? n : 1) : E;
+    return (int)((n + active - 1) / active);
+}
+
 int pick_token_tile(int n, int E) {
     // Test override: MOE_W4A16_TOKEN_TILE = 16, 32, 64, 128 or 160.
     static const int forced = [] {
@@ -31,8 +37,7 @@ int pick_token_tile(int n, int E) {
     // one 128-row tile per SM no longer fits in L2 at once.  Measured on the
     // E = 128 / E = 384 workloads: 32 beats 16 at 16 rows per expert, 64
     // beats 128 at 85 and 128 rows, 128 wins at 341; at 22 rows 32 beats 64.
-    const int active = n < E ? (n > 0 ? n : 1) : E;
-    const int avg = (n + active - 1) / active;
+    const int avg = rows_per_active_expert(n, E);
     const int want = avg + avg / 4;
     int nt = 16;
     while (nt < want && nt < 128) nt <<= 1;
@@ -81,9 +86,15 @@ bool use_decode_kernel(int64_t n, int nt) {
 // GB300, 80 against 64 rows: E = 128 M = 1024 (64 rows per expert) down
 // GEMM 206 -> 168 us, M = 2048 332 -> 315 us, Zipf prefill M = 16384
 // 5.32 -> 5.02 ms, E = 384 M = 4096 1.78 -> 1.76 ms.
-int down_token_tile(int nt, int H) {
+int down_token_tile(int nt, int H, int64_t n, int E) {
     static const bool forced = std::getenv("MOE_W4A16_TOKEN_TILE") != nullptr;
     if (nt == 160 || (nt == 128 && !forced)) return tc_pair_mode(MOE_PACK_W2, 80, H) ? 80 : 64;
+    // At most 3 rows per active expert (decode batches): 8-row down tiles.
+    // A stage then holds 4 KiB of hi and lo rows next to the 9 KiB weight
+    // block, so 16 stages fit where the 16-row tiles' 17 KiB stages left
+    // room for 12, and the weight stream keeps more bytes in flight (12 -> 8
+    // stages of the 16-row tiles cost 7% at decode M = 9 and 90).
+    if (!forced && nt == 16 && rows_per_active_expert(n, E) <= 3) return 8;
     return (forced || nt <= 64) ? nt : 64;
 }
 
@@ -107,8 +118,9 @@ FwdLayout fwd_layout(int M, int k, int E, int H, int I) {
     const size_t n = (size_t)M * k;
     FwdLayout l;
     l.nt = pick_token_tile((int)n, E);
-    l.nt2 = down_token_tile(l.nt, H);
     l.fused = use_decode_kernel((int64_t)n, l.nt);
+    // (the single small-batch kernel takes 16-row tiles in both GEMMs)
+    l.nt2 = l.fused ? l.nt : down_token_tile(l.nt, H, (int64_t)n, E);
     l.max_tok_tiles = (int)(n / l.nt) + (n < (size_t)E ? (int)n : E) + 1;
     l.max_tok_tiles2 = (int)(n / l.nt2) + (n < (size_t)E ? (int)n : E) + 1;
     l.grid = kMaxGrid;

@@ -153,7 +153,9 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     constexpr bool kCat = (KIND == MOE_PACK_W2) && (NT <= 64 || NT == 80);  // == stacked_hi_lo(NT)
     constexpr int kAB = a_buffers(NT, STAGES, DQG);  // TMEM A buffers in use
     constexpr int kAccBase = kAB * kACols;
-    constexpr int kAccCols = kCat ? 2 * NT : NT;              // columns per accumulator
+    // columns per accumulator (at least 32 stacked ones: the epilogue reads
+    // 16-column blocks, the lo block of an 8-row tile from column 8)
+    constexpr int kAccCols = kCat ? (2 * NT > 32 ? 2 * NT : 32) : NT;
     // CTA pairs with two MMA issuers: tensor memory holds one accumulator
     // pair (double-buffered), not one per issuer, so the issuers take the
     // chunks in turns and accumulate into the same one (below)
@@ -801,7 +803,8 @@ struct Config {
     //    warp cost 1-2%, so it keeps one issuer there).
     static constexpr int kDq = kWide ? 6 : (k160 ? 3 : ((kStages % 4 == 0) ? 4 : 2));
     static constexpr int kAB = a_buffers(NT, kStages, kDq);
-    static constexpr int kAccCols = (KIND == MOE_PACK_W2 && (NT <= 64 || NT == 80)) ? 2 * NT : NT;
+    static constexpr int kAccCols = (KIND == MOE_PACK_W2 && (NT <= 64 || NT == 80))
+                                        ? (2 * NT > 32 ? 2 * NT : 32) : NT;
     // (two issuers with accumulators of their own need the A buffers and
     // stages to split evenly between them)
     static constexpr int kMma = (CG == 2) ? (KIND == MOE_PACK_W13 ? 2 : 1)
@@ -842,6 +845,9 @@ bool pick_nt(bool pair, KernelFn *fn, size_t *smem, int *threads) {
 template <int KIND>
 bool pick(int nt, bool pair, KernelFn *fn, size_t *smem, int *threads) {
     switch (nt) {
+        case 8:  // down only (decode batches)
+            if constexpr (KIND == MOE_PACK_W2) return pick_cfg<KIND, 8, 1>(fn, smem, threads);
+            return false;
         case 16: return pick_nt<KIND, 16>(pair, fn, smem, threads);
         case 32: return pick_nt<KIND, 32>(pair, fn, smem, threads);
         case 64: return pick_nt<KIND, 64>(pair, fn, smem, threads);

@@ -102,7 +102,7 @@ struct FwdLayout {
 // Token rows per tile for a batch of n = M*k slots over E experts: for the
 // gate+up GEMM, and for the down GEMM given the former.
 int pick_token_tile(int n, int E);
-int down_token_tile(int nt, int H);
+int down_token_tile(int nt, int H, int64_t n, int E);
 // Whether a batch of n slots with gate+up token tiles of nt rows runs as the
 // single small-batch kernel.
 bool use_decode_kernel(int64_t n, int nt);
