@@ -59,10 +59,10 @@ FUSED_KERNEL = "decode_fused"   # opt-in: the whole layer in one kernel
 # longer describes the kernel and the bench reports traffic as null.
 TRAFFIC_CAPTURE = {
     "kernel": "gemm_gate_up",
-    "sources_sha256": "9275c6c5618209509aad579bd8033ffcccee035f80c42a8467d506015b49eaa9",
+    "sources_sha256": "98047959b433e1993eff33fae6ef0a5d0d333f92b119b994cec5fe0ddeca7126",
     "workload": "decode_e384_h7168_i2048_top8",
-    "bytes_per_launch": {1: 132318720 + 2753536, 9: 1091142656 + 563712,
-                         90: 5559584256 + 2228736},
+    "bytes_per_launch": {1: 132315904 + 2792704, 9: 1091206656 + 750592,
+                         90: 5559540224 + 2058240},
     "profile": "profiles/dram_gemm_gate_up_decode_e384_m1_9_90.md",
 }
 KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "tc_common.cuh", "sm100.cuh", "moe_internal.h",
