@@ -25,20 +25,23 @@
 //    rows (one tensor copy, 128-byte swizzle) into a ring of shared-memory
 //    stages.
 //  * Dequantisation warpgroups (four, or six in the gate+up GEMM with small
-//    token tiles; each takes every fourth or sixth chunk) turn codes into
+//    token tiles, three with the 160/80-row pair tiles; each takes every
+//    fourth, sixth or third chunk) turn codes into
 //    exact fp16 weights, (q - 8) * scale, one weight row per thread, and
 //    write them straight into tensor memory with tcgen05.st.  That tensor
 //    memory is the A operand of tcgen05.mma, so dequantised weights never
 //    touch shared memory.
-//  * One or two MMA warps (alternate chunks, each with its own accumulator)
-//    issue tcgen05.mma (kind::f16, M = 128, N = token rows of the tile
-//    rounded up to 16, K = 16) from one elected thread, accumulating in
-//    tensor memory; the down GEMM multiplies the hi and the lo halves of a
-//    (stacked into one B operand for small token tiles).
+//  * One or two MMA warps (alternate chunks, each with its own accumulator,
+//    or on the gate+up GEMM's CTA pairs taking turns on one) issue
+//    tcgen05.mma (kind::f16, M = 128, N = token rows of the tile rounded up
+//    to 16, K = 16) from one elected thread, accumulating in tensor memory;
+//    the down GEMM multiplies the hi and the lo halves of a (stacked into
+//    one B operand for small token tiles: 8 rows at decode, whose stages
+//    leave room for 16 of them).
 //  * An epilogue warpgroup drains the (double-buffered) accumulators while
 //    the next tile is being computed.
-//  * Large token tiles (128 rows in the gate+up GEMM, 64 in the down GEMM)
-//    run on CTA pairs (clusters of two, tcgen05 cta_group::2): a work tile
+//  * Large token tiles (128/160 rows in the gate+up GEMM, 64/80 in the down
+//    GEMM) run on CTA pairs (clusters of two, tcgen05 cta_group::2): a work tile
 //    is two neighbouring weight tiles, one per CTA, and one M = 256 MMA
 //    covers both, so each SM loads only half of the token operand.  One SM
 //    alone could not take in its 32 KiB of token rows per chunk as fast as
