@@ -15,6 +15,8 @@ namespace moe {
 
 constexpr int kMaxGrid = 256;  // bound on the GEMM grid used to size workspaces
 
+static bool decode_kernel_enabled();
+
 // Rows per active expert if routing spreads the n slots evenly (rounded up).
 static int rows_per_active_expert(int64_t n, int E) {
     const int64_t active = n < E ? (n > 0 ? n : 1) : E;
@@ -29,6 +31,14 @@ int pick_token_tile(int n, int E) {
         return (t == 16 || t == 32 || t == 64 || t == 128 || t == 160) ? t : 0;
     }();
     if (forced) return forced;
+    // At most 3 rows per active expert (decode batches) and at least 32
+    // slots: 8-row tiles, whose 11 KiB stages (2 KiB of token rows next to
+    // the 9 KiB weight block) leave room for 18 stages where 16-row tiles
+    // fit 12, so more weight bytes stay in flight (E = 384 M = 90 gate+up
+    // GEMM 858 -> 827 us, M = 9 180 -> 178 us; at M = 1, 8 slots, 34.8 ->
+    // 36.8 us, so the smallest batches keep 16 rows).  (The opt-in single
+    // small-batch kernel takes 16-row tiles.)
+    if (n >= 32 && rows_per_active_expert(n, E) <= 3 && !decode_kernel_enabled()) return 8;
     // Rows per active expert if routing spreads the slots evenly.  The tile
     // is sized for about 1.25x that, so that most experts' rows fit in one
     // tile (every extra token tile streams the expert's weights again), but
@@ -94,7 +104,7 @@ int down_token_tile(int nt, int H, int64_t n, int E) {
     // block, so 16 stages fit where the 16-row tiles' 17 KiB stages left
     // room for 12, and the weight stream keeps more bytes in flight (12 -> 8
     // stages of the 16-row tiles cost 7% at decode M = 9 and 90).
-    if (!forced && nt == 16 && rows_per_active_expert(n, E) <= 3) return 8;
+    if (!forced && nt <= 16 && rows_per_active_expert(n, E) <= 3) return 8;
     return (forced || nt <= 64) ? nt : 64;
 }
 

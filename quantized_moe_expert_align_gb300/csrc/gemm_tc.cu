@@ -158,7 +158,8 @@ __global__ void __launch_bounds__(threads_for(DQG, NPROD, MMAW), 1)
     constexpr int kAccBase = kAB * kACols;
     // columns per accumulator (at least 32 stacked ones: the epilogue reads
     // 16-column blocks, the lo block of an 8-row tile from column 8)
-    constexpr int kAccCols = kCat ? (2 * NT > 32 ? 2 * NT : 32) : NT;
+    // (8-row gate+up tiles: the MMA's N is 16)
+    constexpr int kAccCols = kCat ? (2 * NT > 32 ? 2 * NT : 32) : (NT < 16 ? 16 : NT);
     // CTA pairs with two MMA issuers: tensor memory holds one accumulator
     // pair (double-buffered), not one per issuer, so the issuers take the
     // chunks in turns and accumulate into the same one (below)
@@ -787,7 +788,8 @@ struct Config {
     // pairs): 6 stages of 29 KiB, 3 dequant warpgroups, whose 3 A buffers
     // leave room for the two accumulators
     static constexpr bool k160 = NT == 160 || NT == 80;
-    static constexpr int kStages = kWide ? 12 : (k160 ? 6 : (kFit & ~1));
+    // (18 stages of the 8-row gate+up tiles' 11 KiB)
+    static constexpr int kStages = kWide ? (kFit >= 18 ? 18 : 12) : (k160 ? 6 : (kFit & ~1));
     // Warp roles.  Each mbarrier wait costs a shared-memory round trip of
     // over a hundred cycles even when the phase is complete, and every
     // instruction of the small control loops waits behind the dequantisation
@@ -807,7 +809,7 @@ struct Config {
     static constexpr int kDq = kWide ? 6 : (k160 ? 3 : ((kStages % 4 == 0) ? 4 : 2));
     static constexpr int kAB = a_buffers(NT, kStages, kDq);
     static constexpr int kAccCols = (KIND == MOE_PACK_W2 && (NT <= 64 || NT == 80))
-                                        ? (2 * NT > 32 ? 2 * NT : 32) : NT;
+                                        ? (2 * NT > 32 ? 2 * NT : 32) : (NT < 16 ? 16 : NT);
     // (two issuers with accumulators of their own need the A buffers and
     // stages to split evenly between them)
     static constexpr int kMma = (CG == 2) ? (KIND == MOE_PACK_W13 ? 2 : 1)
@@ -848,9 +850,7 @@ bool pick_nt(bool pair, KernelFn *fn, size_t *smem, int *threads) {
 template <int KIND>
 bool pick(int nt, bool pair, KernelFn *fn, size_t *smem, int *threads) {
     switch (nt) {
-        case 8:  // down only (decode batches)
-            if constexpr (KIND == MOE_PACK_W2) return pick_cfg<KIND, 8, 1>(fn, smem, threads);
-            return false;
+        case 8: return pick_cfg<KIND, 8, 1>(fn, smem, threads);  // decode batches
         case 16: return pick_nt<KIND, 16>(pair, fn, smem, threads);
         case 32: return pick_nt<KIND, 32>(pair, fn, smem, threads);
         case 64: return pick_nt<KIND, 64>(pair, fn, smem, threads);

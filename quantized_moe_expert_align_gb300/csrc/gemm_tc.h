@@ -7,7 +7,7 @@
 
 namespace moe {
 
-constexpr int kMaxStages = 16;
+constexpr int kMaxStages = 18;
 
 struct TcArgs {
     const uint8_t *w;            // prepacked weights (header included)
