@@ -85,6 +85,15 @@ def test_cta_pairs_160_row_tiles(gpu):
     assert _run_counts(synth.Layer(20, 256, 256, 1), _RAGGED_160, seed=2) == 160
 
 
+def test_eight_row_tiles_with_a_heavy_expert(gpu):
+    """A decode-sized batch (at least 32 slots, at most 3 rows per active
+    expert) runs both GEMMs on 8-row token tiles; one expert spans five of
+    them, the last ragged.  Every token's output and every slot's act and y."""
+    import quantized_moe_expert_align_gb300 as moe
+    assert _run_counts(synth.Layer(32, 256, 256, 1), [37] + [1] * 31, seed=3) == 8
+    assert moe.moe_w4a16_get_diag()["token_tile2"] == 8
+
+
 def test_e1024_round_robin(gpu):
     import quantized_moe_expert_align_gb300 as moe
     L = synth.Layer(1024, 256, 128, 8)
