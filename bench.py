@@ -59,10 +59,10 @@ FUSED_KERNEL = "decode_fused"   # opt-in: the whole layer in one kernel
 # longer describes the kernel and the bench reports traffic as null.
 TRAFFIC_CAPTURE = {
     "kernel": "gemm_gate_up",
-    "sources_sha256": "98047959b433e1993eff33fae6ef0a5d0d333f92b119b994cec5fe0ddeca7126",
+    "sources_sha256": "bd099faca5e098c8f0b518a325138edde1d2ed479ece9339616085d52d719294",
     "workload": "decode_e384_h7168_i2048_top8",
-    "bytes_per_launch": {1: 132315904 + 2792704, 9: 1091206656 + 750592,
-                         90: 5559540224 + 2058240},
+    "bytes_per_launch": {1: 132329216 + 2752768, 9: 1091149312 + 1076736,
+                         90: 5559584512 + 2606592},
     "profile": "profiles/dram_gemm_gate_up_decode_e384_m1_9_90.md",
 }
 KERNEL_SOURCES = ["gemm_tc.cu", "gemm_tc.h", "tc_common.cuh", "sm100.cuh", "moe_internal.h",
