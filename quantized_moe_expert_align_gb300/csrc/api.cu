@@ -38,7 +38,9 @@ int pick_token_tile(int n, int E) {
     // GEMM 858 -> 827 us, M = 9 180 -> 178 us; at M = 1, 8 slots, 34.8 ->
     // 36.8 us, so the smallest batches keep 16 rows).  (The opt-in single
     // small-batch kernel takes 16-row tiles.)
-    if (n >= 32 && rows_per_active_expert(n, E) <= 3 && !decode_kernel_enabled()) return 8;
+    if (n >= 32 && rows_per_active_expert(n, E) <= 3 &&
+        !(decode_kernel_enabled() && n <= kDecodeMaxSlots))
+        return 8;
     // Rows per active expert if routing spreads the slots evenly.  The tile
     // is sized for about 1.25x that, so that most experts' rows fit in one
     // tile (every extra token tile streams the expert's weights again), but
