@@ -75,10 +75,10 @@ static int test_no_copies() {
 // Opt-in switch, read once per process: MOE_W4A16_DECODE_FUSED=1 runs
 // batches of at most kDecodeMaxSlots slots (16-row token tiles) as the single
 // small-batch kernel.  Off by default: on one GB300 that kernel measured
-// 7-10% slower than the five kernels at M = 1, 9 and 16 (E = 384), its
-// prologue and grid barrier costing about 10 us and its weight stream
-// running at about 0.35 us per 128-element chunk per SM against 0.24-0.27
-// for the separate GEMMs.
+// slower than the four kernels of the small-batch path (E = 384, M = 1 / 9:
+// 74 / 330 us against 62 / 285 us), its prologue and grid barrier costing
+// about 10 us and its weight stream running slower per 128-element chunk
+// than the separate GEMMs'.
 static bool decode_kernel_enabled() {
     static const bool on = [] {
         const char *v = std::getenv("MOE_W4A16_DECODE_FUSED");
