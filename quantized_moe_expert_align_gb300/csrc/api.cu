@@ -184,8 +184,8 @@ moe_status_t check_device() {
         cudaGetLastError();
         return MOE_ERR_UNSUPPORTED_DEVICE;
     }
-    static int verdict[64] = {0};  // 0 unknown, 1 supported, 2 not
-    if (dev >= 0 && dev < 64 && verdict[dev]) return verdict[dev] == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED_DEVICE;
+    static int support[64] = {0};  // 0 unknown, 1 supported, 2 not
+    if (dev >= 0 && dev < 64 && support[dev]) return support[dev] == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED_DEVICE;
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
@@ -193,7 +193,7 @@ moe_status_t check_device() {
         return MOE_ERR_UNSUPPORTED_DEVICE;
     }
     const bool ok = (major == 10 && minor == 3);
-    if (dev >= 0 && dev < 64) verdict[dev] = ok ? 1 : 2;
+    if (dev >= 0 && dev < 64) support[dev] = ok ? 1 : 2;
     return ok ? MOE_OK : MOE_ERR_UNSUPPORTED_DEVICE;
 }
 
